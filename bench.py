@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark of the DeepSeekMoE layer forward with aux-loss-free routing on B300.
+
+One step = the whole hot path on one batch: route (router GEMM + sigmoid + bias
++ top-k + gates + load histogram), permute, grouped SwiGLU expert GEMMs (routed
++ shared), combine, and the bias update from the step's load.  Default
+workload: the V3-shaped layer (T=8192 tokens, d=7168, 256 routed + 1 shared
+experts, top-8, I=2048, bf16 with FP32 accumulation).  Inputs are seeded and
+synthetic and resident in HBM; 22.6 GB of expert weights are streamed every
+step, far more than the 126 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3|mid|v3fp8|skew|tiny]
+    python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+
+Prints one JSON line (rank 0).  Multi-GPU (torchrun, one rank per GPU): every
+rank runs its own T tokens (weak scaling) and the per-expert counts are summed
+across ranks before the bias update, so every replica keeps the same bias.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (d=7168, 256 routed + 1 shared experts, top-8)"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--config", default="v3")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+        idx = vis if vis.isdigit() else "0"
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9 and r[0].strip() == idx] or \
+               [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_experts=6, n_tok=512):
+    """Times the oracle on the host cores on a bounded sample of the workload and
+    extrapolates to the whole step (tokens/s).  Router and permutation run on all T
+    tokens; the expert FFN runs on a sample of routed experts (all their tokens)
+    plus the shared experts on n_tok tokens, scaled by FLOPs; combine on all tokens."""
+    import numpy as np
+
+    from oracle import moe_oracle as O
+
+    def f64(t):
+        return t.detach().float().cpu().double().numpy()
+
+    xn = f64(x)
+    wrn = f64(w_router)
+    bn = bias.detach().cpu().numpy()
+    on = None if logit_offset is None else logit_offset.cpu().numpy()
+    t0 = time.perf_counter()
+    r = O.route(xn, wrn, bn, cfg.k, on)
+    p = O.permutation(r["idx"], cfg.E)
+    t_route = time.perf_counter() - t0
+    # expert FFN sample (weights converted outside the timed part)
+    rng = np.random.default_rng(0)
+    experts = rng.choice(cfg.E, size=min(n_experts, cfg.E), replace=False)
+    t_ffn, flops_done = 0.0, 0.0
+    for e in list(experts) + list(range(cfg.E, cfg.E + cfg.S)):
+        a, b = f64(wgu[e]), f64(wd[e])
+        if e < cfg.E:
+            rows = xn[p["perm_token"][p["offsets"][e]:p["offsets"][e + 1]]]
+        else:
+            rows = xn[:n_tok]
+        t1 = time.perf_counter()
+        O.swiglu_expert(rows, a, b)
+        t_ffn += time.perf_counter() - t1
+        flops_done += 2.0 * rows.shape[0] * 3 * cfg.d * cfg.I
+    y = np.zeros((cfg.T * cfg.k + cfg.S * cfg.T, cfg.d), dtype=np.float32)
+    t2 = time.perf_counter()
+    O.combine(y, r["gate"], p["inv_pos"], cfg.T, cfg.k, cfg.S)
+    O.bias_update(bn, p["counts"], cfg.T, cfg.k, cfg.gamma)
+    t_comb = time.perf_counter() - t2
+    t_total = t_route + t_comb + t_ffn * (cfg.expert_flops() / flops_done)
+    cores = len(os.sched_getaffinity(0))
+    return {
+        "value": cfg.T / t_total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        "sample": (f"{cfg.name}: router+permute+combine+bias update on all {cfg.T} tokens; expert FFN on "
+                   f"{len(experts)} routed experts (all their tokens) + {cfg.S} shared on {n_tok} tokens, "
+                   f"extrapolated by FLOPs ({t_total:.1f} s per step extrapolated, "
+                   f"{t_route + t_comb + t_ffn:.1f} s measured)"),
+        "seconds_measured": t_route + t_comb + t_ffn,
+    }
+
+
+def _setup_dist():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def run_reference(args):
+    """The oracle (CPU) on this arm's workload, each step a bounded sample."""
+    import torch
+
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = I.CONFIGS[args.config]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = I.make_x(cfg, dev)
+    wr = I.make_router(cfg, dev)
+    b = I.make_bias(cfg, dev)
+    off = I.make_logit_offset(cfg, dev)
+    wgu, wd = (None, None)
+    wgu_l, wd_l = {}, {}
+    n = cfg.E + cfg.S
+
+    class Lazy:
+        def __init__(self, which):
+            self.which = which
+
+        def __getitem__(self, e):
+            if e not in wgu_l:
+                wgu_l.clear()
+                wd_l.clear()
+                a, bb = I.make_expert(cfg, e, dev)
+                wgu_l[e], wd_l[e] = a, bb
+            return wgu_l[e] if self.which == 0 else wd_l[e]
+
+    wgu, wd = Lazy(0), Lazy(1)
+    assert n > 0
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=1, n_tok=64)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=2, n_tok=128))
+    wall = time.perf_counter() - t0
+    v = statistics.median([c["value"] for c in vals])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{cfg.name} T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} k={cfg.k} "
+                                                    f"I={cfg.I}", "l2": "inputs larger than L2"},
+        "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v,
+                         "unit": "tokens/s"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_moe_layer_12_b300 import binding as B
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    world, rank, local = _setup_dist()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    cfg = I.CONFIGS[args.config]
+    cfg_r = cfg.with_(seed=cfg.seed + rank)  # each rank its own tokens (weak scaling); same weights
+    B.load()
+    fp8 = cfg.fp8
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)
+    shape_g = B.make_shape(cfg.T * world, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)  # bias update: global load
+    x = I.make_x(cfg_r, dev)
+    wr = I.make_router(cfg, dev)
+    bias = I.make_bias(cfg, dev)
+    off = I.make_logit_offset(cfg, dev)
+    wgu, wd = I.make_experts(cfg, dev)
+    wgu_s = wd_s = None
+    if fp8:
+        wgu_b, wd_b = wgu, wd
+        wgu, wgu_s = B.moe_quantize_weights_fp8(wgu_b)
+        wd, wd_s = B.moe_quantize_weights_fp8(wd_b)
+        del wgu_b, wd_b
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    ws = B.alloc_workspace(shape, dev)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        idx, gate, counts, offsets = B.moe_route(shape, x, wr, bias, off, ws=ws)
+        xp, xps, ptok, inv = B.moe_permute(shape, x, idx, offsets, ws=ws)
+        if ev is not None:
+            ev[0].record(stream)
+        y = B.moe_expert_ffn(shape, xp, xps, x, offsets, wgu, wd, wgu_s, wd_s, ws=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        B.moe_combine(shape, y, gate, inv, out=out)
+        if world > 1:
+            dist.all_reduce(counts)
+        B.moe_bias_update(shape_g, counts, bias, cfg.gamma)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks()
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ck = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    ffn_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    status = B.moe_get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {B.STATUS.get(status)} after the timed region")
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        outh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        ch = torch.empty(cfg.E, dtype=torch.int32).pin_memory()
+        xd = torch.empty_like(x)
+        counts_d = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            B.moe_forward(shape, xd, wr, bias, wgu, wd, logit_offset=off, w_gu_scale=wgu_s, w_down_scale=wd_s,
+                          gamma=cfg.gamma, update_bias=(world == 1), ws=ws, out=out, routing_out=False)
+            outh.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b_)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * cfg.T * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
+               "ms_per_step": e_ms / args.steps}
+        del ch
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    pk, pk_src = _peaks()
+    flops = cfg.expert_flops()
+    ffn_avg_s = statistics.mean(ffn_ms) / 1e3
+    achieved = flops / ffn_avg_s / 1e12
+    peak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    line = {
+        "metric": METRIC,
+        "value": world * cfg.T * args.steps / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8-e4m3 (fp32 acc)" if fp8 else "bf16 (fp32 acc)",
+        "data": "synthetic (seeded, random-init weights of the layer's shape)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T}/GPU d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}",
+                   "global_batch": world * cfg.T, "parallelism": f"dp{world} (token-sharded replicas)",
+                   "l2": "inputs larger than L2 (expert weights streamed every step)"},
+        "expert_gemm_tflops": achieved,
+        "expert_gemm_pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (grouped gate/up+SwiGLU and down GEMMs)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
+                     "traffic": None},
+        "stage_ms": {"expert_ffn": statistics.mean(ffn_ms), "rest": ms / args.steps - statistics.mean(ffn_ms)},
+        "gpu_launches": 9 * args.steps,
+        "clocks": ck,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, x, wr, bias, wgu if not fp8 else I.make_experts(cfg, dev)[0],
+                                                 wd if not fp8 else I.make_experts(cfg, dev)[1], off)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * moe.h -- C ABI of libmoe: the forward pass of a DeepSeekMoE layer with
+ * auxiliary-loss-free (bias-steered) top-k routing, on one B300 (sm_103a).
+ *
+ * The layer, as the pages state it:
+ *   - "DeepSeek-V3 详解" (yudonglee.me), section 2.2: fine-grained routed
+ *     experts plus one always-on shared expert, top-8 of 256 per token;
+ *     section 2.3: a per-expert bias, update speed gamma = 0.001.
+ *   - "deepseek-v3-report" (dynmi.github.io), load-balancing paragraph: the
+ *     bias b_i is added to the routing score, lowered for an overloaded expert
+ *     and raised for an idle one, and stays out of the gradient.
+ *   - "DeepSeek-V3 技术报告要点" (deepseek.csdn.net), section 4.2: the bias is
+ *     moved from the load observed in each batch; section 3 table: hidden
+ *     size 7168, expert intermediate size 2048; section 1: SwiGLU FFN.
+ *   - FP8 path: "DeepSeek-V3 详解", section 4.2 (1x128 activation tiles,
+ *     128x128 weight blocks) and 4.3 (FP32 accumulation).
+ * Where the pages are silent the library takes these readings: affinity
+ * s = sigmoid(x . w_i [+ o_i]); selection by the k largest s + b (descending,
+ * ties to the lower expert index); gate = s / (sum of s over the chosen k);
+ * shared experts ungated; output excludes the residual.
+ *
+ * Conventions for every call:
+ *   - Every pointer is a DEVICE pointer unless stated; the caller owns all
+ *     memory, including the workspace.  The library never allocates or frees.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     none synchronises the host, except moe_get_device_status.
+ *   - Arguments are validated before anything is launched; a non-OK status
+ *     means nothing was enqueued.  No C++ exception crosses the ABI.
+ *   - Row-major tensors must start on a 16-byte boundary.
+ *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 bits;
+ *     FP8 tensors hold OCP E4M3 ("e4m3fn") bytes.
+ *   - Errors found on the device (a wait that timed out, an index out of
+ *     range) are recorded in a status word inside the workspace and read back
+ *     with moe_get_device_status.
+ *   - Shape limits: T >= 0, d % 128 == 0 (128 <= d <= 65536),
+ *     I % 128 == 0 (128 <= I <= 65536), 1 <= E <= 256, 0 <= S <= 8,
+ *     1 <= k <= min(E, 16), (T*k + S*T) * max(d, I) < 2^31.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad shape, bad gamma          */
+  MOE_ERR_UNSUPPORTED = 2, /* valid layer, outside this library's limits  */
+  MOE_ERR_ALIGNMENT = 3,   /* a tensor does not start on 16 bytes         */
+  MOE_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required  */
+  MOE_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed         */
+  MOE_ERR_TIMEOUT = 6,     /* device: a bounded wait gave up              */
+  MOE_ERR_DEVICE = 7       /* device: an index or count was inconsistent  */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_dtype_t;
+
+/* T tokens, d model width, E routed experts, S shared experts, k experts
+ * chosen per token, I expert intermediate size; dtype of the expert GEMMs. */
+typedef struct {
+  int T, d, E, S, k, I;
+  moe_dtype_t dtype;
+} moe_shape_t;
+
+/* A CUDA stream (same type as cudaStream_t). */
+typedef struct CUstream_st* moe_stream_t;
+
+/* Bytes of workspace every call below needs for `shape` (the maximum over all
+ * calls, so one buffer serves them all); 0 if the shape is invalid.  The
+ * workspace must start on 256 bytes and its first 256 bytes (the device
+ * status word) must be zero before its first use; the rest needs no
+ * initialisation. */
+MOE_API size_t moe_workspace_bytes(const moe_shape_t* shape);
+
+/* Router ("deepseek-v3-report", load-balancing paragraph; "DeepSeek-V3 详解"
+ * 2.3).  For every token t and routed expert i:
+ *     z = x[t] . w_router[i] (+ logit_offset[i]),  s = sigmoid(z),
+ *     chosen = the k largest s + bias[i] (descending, ties -> lower i),
+ *     gate   = s[chosen] / sum_j s[chosen_j].
+ *   x            bf16 [T, d]          token activations (input)
+ *   w_router     bf16 [E, d]          router weight (input)
+ *   bias         f32  [E]             selection bias b (input; selection only)
+ *   logit_offset f32  [E] or NULL     per-expert logit offset added to z
+ *   topk_idx     int32 [T, k]  out    chosen experts
+ *   topk_gate    f32  [T, k]   out    gates
+ *   counts       int32 [E]     out    tokens routed to each expert (load)
+ *   offsets      int32 [E+1]   out    exclusive prefix sum of counts
+ * z is accumulated in FP32 on the tensor cores; s, s + b and the gates are
+ * FP32.  Deterministic run to run. */
+MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_router,
+                       const float* bias, const float* logit_offset, int32_t* topk_idx,
+                       float* topk_gate, int32_t* counts, int32_t* offsets, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch: group the (token, slot) pairs by expert, tokens ascending inside
+ * an expert (the single-GPU form of the all-to-all dispatch in "DeepSeek-V3
+ * Overview and Key Innovations", Training Infrastructure and Optimization).
+ *   x            bf16 [T, d]          (input)
+ *   topk_idx     int32 [T, k]         (input, values in [0, E))
+ *   offsets      int32 [E+1]          (input, from moe_route)
+ *   x_perm       [T*k, d]      out    bf16, or E4M3 bytes when dtype = FP8
+ *   x_perm_scale f32 [T*k, d/128] out FP8 only (1x128 tile scales), else NULL
+ *   perm_token   int32 [T*k]   out    token of each permuted row
+ *   inv_pos      int32 [T, k]  out    permuted row of (t, j)
+ * FP8 quantisation (scale = amax/448 per 1x128 tile, RNE, saturating) is
+ * done on the way.  Inconsistent idx/offsets set MOE_ERR_DEVICE. */
+MOE_API moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t* topk_idx,
+                         const int32_t* offsets, void* x_perm, float* x_perm_scale,
+                         int32_t* perm_token, int32_t* inv_pos, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Experts ("DeepSeek-V3 技术报告要点" section 1 and section 3 table): for every
+ * routed expert e its rows of x_perm, and for every shared expert s all T rows
+ * of x, go through the SwiGLU FFN
+ *     h = silu(X W_gate^T) * (X W_up^T),   Y = h W_down^T.
+ *   x_perm      [T*k, d]   bf16 / E4M3 (input, from moe_permute)
+ *   x_perm_scale f32 [T*k, d/128] FP8 only, else NULL
+ *   x           bf16 [T, d]           input of the shared experts
+ *   offsets     int32 [E+1]           routed group boundaries in x_perm
+ *   w_gate_up   [E+S, 2I, d]  bf16 / E4M3: rows 0..I-1 gate, I..2I-1 up;
+ *               experts E..E+S-1 are the shared experts
+ *   w_gu_scale  f32 [E+S, 2I/128, d/128]  FP8 only (128x128 block scales)
+ *   w_down      [E+S, d, I]   bf16 / E4M3
+ *   w_down_scale f32 [E+S, d/128, I/128]  FP8 only
+ *   y           bf16 [T*k + S*T, d] out   rows 0..T*k-1 follow x_perm; row
+ *               T*k + s*T + t is shared expert s on token t
+ * FP32 accumulation; h is rounded to bf16 (BF16) or quantised per 1x128 to
+ * E4M3 (FP8) before the down projection. */
+MOE_API moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const float* x_perm_scale,
+                            const void* x, const int32_t* offsets, const void* w_gate_up,
+                            const float* w_gu_scale, const void* w_down, const float* w_down_scale,
+                            void* y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: out[t] = sum_s y[T*k + s*T + t] + sum_j topk_gate[t, j] * y[inv_pos[t, j]]
+ * (shared experts first, then slots j = 0..k-1, FP32 sum, bf16 store).
+ *   y bf16 [T*k + S*T, d]; topk_gate f32 [T, k]; inv_pos int32 [T, k];
+ *   out bf16 [T, d] (out). */
+MOE_API moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* topk_gate,
+                         const int32_t* inv_pos, void* out, moe_stream_t stream);
+
+/* Bias update ("DeepSeek-V3 详解" 2.3, "deepseek-v3-report"):
+ *     bias[i] += gamma * sign(T*k/E - counts[i]),  sign(0) = 0,
+ * the sign decided on integers, the add in FP32.  In place on `bias` [E]. */
+MOE_API moe_status_t moe_bias_update(const moe_shape_t* shape, const int32_t* counts, float* bias,
+                             float gamma, moe_stream_t stream);
+
+/* The whole layer: moe_route, moe_permute, moe_expert_ffn, moe_combine and,
+ * when update_bias != 0, moe_bias_update with this batch's counts (after the
+ * routing has used the old bias).  topk_idx, topk_gate and counts are optional
+ * outputs (NULL keeps them in the workspace).  All intermediates live in `ws`. */
+MOE_API moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_router,
+                         float* bias, const float* logit_offset, const void* w_gate_up,
+                         const float* w_gu_scale, const void* w_down, const float* w_down_scale,
+                         void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                         float gamma, int update_bias, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* FP8 weight preparation ("DeepSeek-V3 详解" 4.2): quantise `w` bf16
+ * [G, N, K] (N % 128 == 0, K % 128 == 0) per 128x128 block to E4M3 `w_q`
+ * [G, N, K] with f32 scales `w_scale` [G, N/128, K/128] (scale = amax/448,
+ * 1 for an all-zero block).  Used once, before the FP8 layer runs. */
+MOE_API moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q,
+                                      float* w_scale, moe_stream_t stream);
+
+/* Reads (synchronising `stream`) and clears the device status word in `ws`:
+ * MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the read
+ * itself fails).  `ws` must be a workspace used by the calls above. */
+MOE_API moe_status_t moe_get_device_status(void* ws, moe_stream_t stream);
+
+/* Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing will complete, with a limit of `limit_us` microseconds
+ * (1..1000000), after which it records MOE_ERR_TIMEOUT in `ws` and exits.
+ * Used to check failure detection without hanging the GPU. */
+MOE_API moe_status_t moe_debug_wait_timeout(void* ws, unsigned limit_us, moe_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+/* Library version, e.g. "libmoe 0.1 sm_103a". */
+MOE_API const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -227,3 +227,15 @@ def max_rel_err(out, ref) -> float:
     ref = _f64(ref)
     rms = np.sqrt(np.mean(ref * ref))
     return float(np.max(np.abs(out - ref)) / rms)
+
+
+def combine(y, gate, inv_pos, T, k, S) -> np.ndarray:
+    """out[t] = sum_s y[T*k + s*T + t] + sum_j gate[t, j] * y[inv_pos[t, j]] (float64)."""
+    y = _f64(y)
+    out = np.zeros((T, y.shape[1]), dtype=np.float64)
+    for s_id in range(S):
+        out += y[T * k + s_id * T: T * k + (s_id + 1) * T]
+    g = _f64(gate)
+    for j in range(k):
+        out += g[:, j:j + 1] * y[np.asarray(inv_pos)[:, j]]
+    return out

@@ -1,0 +1,243 @@
+"""Thin Python binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function takes torch CUDA tensors, checks dtype / shape / device /
+contiguity, allocates outputs with torch, and calls the C ABI with raw device
+pointers and the current CUDA stream.  No arithmetic of the layer happens here:
+if libmoe.so is missing the calls raise; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_BF16, MOE_FP8_E4M3 = 0, 1
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
+
+# every symbol include/moe.h declares
+EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+           "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
+           "moe_debug_wait_timeout", "moe_status_string", "moe_version"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("E", ctypes.c_int), ("S", ctypes.c_int),
+                ("k", ctypes.c_int), ("I", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+_SIGS = {
+    "moe_workspace_bytes": (_SZ, [ctypes.POINTER(Shape)]),
+    "moe_route": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_combine": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
+    "moe_bias_update": (_I, [ctypes.POINTER(Shape), _P, _P, _F, _P]),
+    "moe_forward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P,
+                         _SZ, _P]),
+    "moe_quantize_weights_fp8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "moe_get_device_status": (_I, [_P, _P]),
+    "moe_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmoe.so not built: {path} (run python -m sparse_moe_layer_12_b300.build)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MoEError(fn, code)
+
+
+def _need(t: torch.Tensor, dtype, shape, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_shape(T, d, E, S, k, I, fp8=False) -> Shape:
+    return Shape(T, d, E, S, k, I, MOE_FP8_E4M3 if fp8 else MOE_BF16)
+
+
+def workspace_bytes(shape: Shape) -> int:
+    return int(load().moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def alloc_workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(shape)
+    if n == 0:
+        raise ValueError("invalid shape")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()  # the device status word starts clear
+    return ws
+
+
+def _act_dtype(shape: Shape):
+    return torch.float8_e4m3fn if shape.dtype == MOE_FP8_E4M3 else torch.bfloat16
+
+
+def moe_route(shape: Shape, x, w_router, bias, logit_offset=None, ws=None):
+    T, d, E, k = shape.T, shape.d, shape.E, shape.k
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(w_router, torch.bfloat16, (E, d), "w_router")
+    _need(bias, torch.float32, (E,), "bias")
+    if logit_offset is not None:
+        _need(logit_offset, torch.float32, (E,), "logit_offset")
+    ws = alloc_workspace(shape, x.device) if ws is None else ws
+    idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    gate = torch.empty(T, k, dtype=torch.float32, device=x.device)
+    counts = torch.empty(E, dtype=torch.int32, device=x.device)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=x.device)
+    _check("moe_route", load().moe_route(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(bias),
+                                         _ptr(logit_offset), _ptr(idx), _ptr(gate), _ptr(counts), _ptr(offsets),
+                                         _ptr(ws), ws.numel(), _stream()))
+    return idx, gate, counts, offsets
+
+
+def moe_permute(shape: Shape, x, topk_idx, offsets, ws=None):
+    T, d, E, k = shape.T, shape.d, shape.E, shape.k
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    ws = alloc_workspace(shape, x.device) if ws is None else ws
+    x_perm = torch.empty(T * k, d, dtype=_act_dtype(shape), device=x.device)
+    scale = (torch.empty(T * k, d // 128, dtype=torch.float32, device=x.device)
+             if shape.dtype == MOE_FP8_E4M3 else None)
+    perm_token = torch.empty(T * k, dtype=torch.int32, device=x.device)
+    inv_pos = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    _check("moe_permute", load().moe_permute(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(offsets),
+                                             _ptr(x_perm), _ptr(scale), _ptr(perm_token), _ptr(inv_pos), _ptr(ws),
+                                             ws.numel(), _stream()))
+    return x_perm, scale, perm_token, inv_pos
+
+
+def moe_expert_ffn(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_down, w_gu_scale=None,
+                   w_down_scale=None, ws=None):
+    T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
+    wdt = _act_dtype(shape)
+    _need(x_perm, wdt, (T * k, d), "x_perm")
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
+    _need(w_down, wdt, (E + S, d, I), "w_down")
+    if shape.dtype == MOE_FP8_E4M3:
+        _need(x_perm_scale, torch.float32, (T * k, d // 128), "x_perm_scale")
+        _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
+        _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
+    ws = alloc_workspace(shape, x.device) if ws is None else ws
+    y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    _check("moe_expert_ffn", load().moe_expert_ffn(
+        ctypes.byref(shape), _ptr(x_perm), _ptr(x_perm_scale), _ptr(x), _ptr(offsets), _ptr(w_gate_up),
+        _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def moe_combine(shape: Shape, y, topk_gate, inv_pos, out=None):
+    T, d, S, k = shape.T, shape.d, shape.S, shape.k
+    _need(y, torch.bfloat16, (T * k + S * T, d), "y")
+    _need(topk_gate, torch.float32, (T, k), "topk_gate")
+    _need(inv_pos, torch.int32, (T, k), "inv_pos")
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=y.device) if out is None else out
+    _check("moe_combine", load().moe_combine(ctypes.byref(shape), _ptr(y), _ptr(topk_gate), _ptr(inv_pos),
+                                             _ptr(out), _stream()))
+    return out
+
+
+def moe_bias_update(shape: Shape, counts, bias, gamma=0.001):
+    _need(counts, torch.int32, (shape.E,), "counts")
+    _need(bias, torch.float32, (shape.E,), "bias")
+    _check("moe_bias_update", load().moe_bias_update(ctypes.byref(shape), _ptr(counts), _ptr(bias),
+                                                     ctypes.c_float(gamma), _stream()))
+    return bias
+
+
+def moe_forward(shape: Shape, x, w_router, bias, w_gate_up, w_down, logit_offset=None, w_gu_scale=None,
+                w_down_scale=None, gamma=0.001, update_bias=False, ws=None, out=None, routing_out=True):
+    """Whole layer; returns (out, topk_idx, topk_gate, counts) (routing tensors None if routing_out=False)."""
+    T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
+    wdt = _act_dtype(shape)
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(w_router, torch.bfloat16, (E, d), "w_router")
+    _need(bias, torch.float32, (E,), "bias")
+    _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
+    _need(w_down, wdt, (E + S, d, I), "w_down")
+    if logit_offset is not None:
+        _need(logit_offset, torch.float32, (E,), "logit_offset")
+    if shape.dtype == MOE_FP8_E4M3:
+        _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
+        _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
+    ws = alloc_workspace(shape, x.device) if ws is None else ws
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=x.device) if out is None else out
+    idx = gate = counts = None
+    if routing_out:
+        idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
+        gate = torch.empty(T, k, dtype=torch.float32, device=x.device)
+        counts = torch.empty(E, dtype=torch.int32, device=x.device)
+    _check("moe_forward", load().moe_forward(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(logit_offset), _ptr(w_gate_up),
+        _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(out), _ptr(idx), _ptr(gate), _ptr(counts),
+        ctypes.c_float(gamma), 1 if update_bias else 0, _ptr(ws), ws.numel(), _stream()))
+    return out, idx, gate, counts
+
+
+def moe_quantize_weights_fp8(w):
+    """bf16 [G, N, K] -> (E4M3 [G, N, K], f32 scales [G, N/128, K/128])."""
+    if not (w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 3 and w.is_contiguous()):
+        raise ValueError("w must be a contiguous CUDA bf16 tensor [G, N, K]")
+    G, N, K = w.shape
+    wq = torch.empty(G, N, K, dtype=torch.float8_e4m3fn, device=w.device)
+    sc = torch.empty(G, N // 128, K // 128, dtype=torch.float32, device=w.device)
+    _check("moe_quantize_weights_fp8", load().moe_quantize_weights_fp8(G, N, K, _ptr(w), _ptr(wq), _ptr(sc),
+                                                                       _stream()))
+    return wq, sc
+
+
+def moe_get_device_status(ws) -> int:
+    return int(load().moe_get_device_status(_ptr(ws), _stream()))
+
+
+def moe_debug_wait_timeout(ws, limit_us: int):
+    _check("moe_debug_wait_timeout", load().moe_debug_wait_timeout(_ptr(ws), limit_us, _stream()))

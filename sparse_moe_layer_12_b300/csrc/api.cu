@@ -1,0 +1,308 @@
+// libmoe C ABI: argument validation, workspace layout, TMA descriptors and the
+// entry points declared in include/moe.h.  Every entry validates before it
+// enqueues anything; compute happens only in the kernels of the other files.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool shape_valid(const moe_shape_t* s) {
+  if (!s) return false;
+  if (s->T < 0 || s->d < 128 || s->I < 128 || s->E < 1 || s->S < 0 || s->k < 1) return false;
+  if (s->d % 128 || s->I % 128 || s->d > 65536 || s->I > 65536) return false;
+  if (s->k > s->E) return false;
+  if (s->dtype != MOE_BF16 && s->dtype != MOE_FP8_E4M3) return false;
+  return true;
+}
+
+static bool shape_supported(const moe_shape_t& s) {
+  if (s.E > kMaxE || s.S > kMaxS || s.k > kMaxK) return false;
+  const long long rows = (long long)s.T * s.k + (long long)s.S * s.T;
+  const long long w = s.d > s.I ? s.d : s.I;
+  if (rows * w >= (1ll << 31)) return false;
+  return true;
+}
+
+WsLayout ws_layout(const moe_shape_t& s) {
+  WsLayout L{};
+  const size_t A = 1024;
+  const size_t Tk = (size_t)s.T * s.k;
+  const size_t rows = Tk + (size_t)s.S * s.T;
+  const bool f8 = s.dtype == MOE_FP8_E4M3;
+  const size_t es = f8 ? 1 : 2;
+  size_t o = 0;
+  L.status = o;      o = align_up(o + 256, A);
+  L.counts = o;      o = align_up(o + 4 * (size_t)s.E, A);
+  L.offsets = o;     o = align_up(o + 4 * ((size_t)s.E + 1), A);
+  L.idx = o;         o = align_up(o + 4 * Tk, A);
+  L.gate = o;        o = align_up(o + 4 * Tk, A);
+  L.perm_token = o;  o = align_up(o + 4 * Tk, A);
+  L.inv_pos = o;     o = align_up(o + 4 * Tk, A);
+  L.sched = o;       o = align_up(o + Schedule::bytes(s.E + s.S), A);
+  L.x_perm = o;      o = align_up(o + Tk * s.d * es, A);
+  L.x_perm_scale = o; o = align_up(o + (f8 ? Tk * (s.d / 128) * 4 : 0), A);
+  L.xq = o;          o = align_up(o + (f8 ? (size_t)s.T * s.d : 0), A);
+  L.xq_scale = o;    o = align_up(o + (f8 ? (size_t)s.T * (s.d / 128) * 4 : 0), A);
+  L.h = o;           o = align_up(o + rows * s.I * es, A);
+  L.h_scale = o;     o = align_up(o + (f8 ? rows * (s.I / 128) * 4 : 0), A);
+  L.y = o;           o = align_up(o + rows * s.d * 2, A);
+  L.total = o;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_ws(const moe_shape_t& s, void* ws, size_t ws_bytes) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < ws_layout(s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || !aligned16(base)) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return f(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                 uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || !aligned16(base)) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * (uint64_t)esize, inner * mid * (uint64_t)esize};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return f(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- debug wait kernel
+
+__global__ void debug_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);  // nothing ever arrives on this barrier
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait(&bar, 0, &abort_flag, status, status + 1, kSiteDebug, limit_ns);
+  }
+  __syncthreads();
+}
+
+moe_status_t launch_debug_wait(void* ws, unsigned limit_us, cudaStream_t st) {
+  debug_wait_kernel<<<1, 32, 0, st>>>(ws_status(ws), (unsigned long long)limit_us * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_TRY(expr)                     \
+  do {                                    \
+    moe_status_t _st = (expr);            \
+    if (_st != MOE_OK) return _st;        \
+  } while (0)
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape_t* shape) {
+  if (!shape_valid(shape)) return 0;
+  return ws_layout(*shape).total;
+}
+
+static moe_status_t validate_shape(const moe_shape_t* shape) {
+  if (!shape_valid(shape)) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(*shape)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_router, const float* bias,
+                       const float* logit_offset, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                       int32_t* offsets, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!x || !w_router || !bias || !topk_idx || !topk_gate || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_ws(s, ws, ws_bytes));
+  return launch_route(s, x, w_router, bias, logit_offset, topk_idx, topk_gate, counts, offsets, ws,
+                      (cudaStream_t)stream);
+}
+
+moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t* topk_idx,
+                         const int32_t* offsets, void* x_perm, float* x_perm_scale, int32_t* perm_token,
+                         int32_t* inv_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!x || !topk_idx || !offsets || !x_perm || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_ws(s, ws, ws_bytes));
+  return launch_permute(s, x, topk_idx, offsets, x_perm, x_perm_scale, perm_token, inv_pos, ws,
+                        (cudaStream_t)stream);
+}
+
+moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const float* x_perm_scale,
+                            const void* x, const int32_t* offsets, const void* w_gate_up,
+                            const float* w_gu_scale, const void* w_down, const float* w_down_scale, void* y,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!x_perm || !x || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3 && (!x_perm_scale || !w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_ws(s, ws, ws_bytes));
+  return launch_expert_ffn(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
+                           y, ws, (cudaStream_t)stream);
+}
+
+moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* topk_gate,
+                         const int32_t* inv_pos, void* out, moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!y || !topk_gate || !inv_pos || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+  return launch_combine(s, y, topk_gate, inv_pos, out, (cudaStream_t)stream);
+}
+
+moe_status_t moe_bias_update(const moe_shape_t* shape, const int32_t* counts, float* bias, float gamma,
+                             moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  if (!counts || !bias) return MOE_ERR_INVALID_ARG;
+  if (!(gamma >= 0.0f) || gamma > 1.0f) return MOE_ERR_INVALID_ARG;
+  return launch_bias_update(*shape, counts, bias, gamma, (cudaStream_t)stream);
+}
+
+moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_router, float* bias,
+                         const float* logit_offset, const void* w_gate_up, const float* w_gu_scale,
+                         const void* w_down, const float* w_down_scale, void* out, int32_t* topk_idx,
+                         float* topk_gate, int32_t* counts, float gamma, int update_bias, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!x || !w_router || !bias || !w_gate_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (update_bias && (!(gamma >= 0.0f) || gamma > 1.0f)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
+    return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_ws(s, ws, ws_bytes));
+  const WsLayout L = ws_layout(s);
+  char* w = static_cast<char*>(ws);
+  int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(w + L.idx);
+  float* gate = topk_gate ? topk_gate : reinterpret_cast<float*>(w + L.gate);
+  int32_t* cnt = counts ? counts : reinterpret_cast<int32_t*>(w + L.counts);
+  int32_t* off = reinterpret_cast<int32_t*>(w + L.offsets);
+  int32_t* ptok = reinterpret_cast<int32_t*>(w + L.perm_token);
+  int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv_pos);
+  void* xp = w + L.x_perm;
+  float* xps = s.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(w + L.x_perm_scale) : nullptr;
+  void* y = w + L.y;
+  cudaStream_t st = (cudaStream_t)stream;
+  MOE_TRY(launch_route(s, x, w_router, bias, logit_offset, idx, gate, cnt, off, ws, st));
+  MOE_TRY(launch_permute(s, x, idx, off, xp, xps, ptok, inv, ws, st));
+  MOE_TRY(launch_expert_ffn(s, xp, xps, x, off, w_gate_up, w_gu_scale, w_down, w_down_scale, y, ws, st));
+  MOE_TRY(launch_combine(s, y, gate, inv, out, st));
+  if (update_bias) MOE_TRY(launch_bias_update(s, cnt, bias, gamma, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q, float* w_scale,
+                                      moe_stream_t stream) {
+  if (G < 0 || N < 0 || K < 0 || N % 128 || K % 128) return MOE_ERR_INVALID_ARG;
+  if ((long long)G * N * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if (G == 0 || N == 0 || K == 0) return MOE_OK;
+  if (!w || !w_q || !w_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(w_q)) return MOE_ERR_ALIGNMENT;
+  return launch_quant_weights(G, N, K, w, w_q, w_scale, (cudaStream_t)stream);
+}
+
+moe_status_t moe_get_device_status(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  int h[2] = {0, 0};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h[0] != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(h), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  switch (h[0]) {
+    case 0: return MOE_OK;
+    case MOE_ERR_TIMEOUT: return MOE_ERR_TIMEOUT;
+    default: return MOE_ERR_DEVICE;
+  }
+}
+
+moe_status_t moe_debug_wait_timeout(void* ws, unsigned limit_us, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  return launch_debug_wait(ws, limit_us, (cudaStream_t)stream);
+}
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_version(void) { return "libmoe 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,388 @@
+// Grouped SwiGLU expert GEMMs on the tcgen05 tensor cores ("DeepSeek-V3 技术报告要点"
+// section 1 (SwiGLU FFN) and section 3 table (expert intermediate 2048);
+// "DeepSeek-V3 详解" 2.2 (256 fine-grained routed experts + 1 shared expert)).
+//
+//   gate/up:  h[r, f] = silu(X[r] . Wg[f]) * (X[r] . Wu[f])   (SiLU*mul fused)
+//   down:     y[r, c] = h[r] . Wd[c]
+//
+// Every routed expert is a group of rows of x_perm; every shared expert is a
+// group over all T rows of x, scheduled in the same persistent launch.
+//
+// Tile shape ("swap AB"): the MMA's M side (128 TMEM lanes) carries weight rows
+// (output features) and its N side carries up to 256 tokens of one group, so a
+// group of n tokens is padded to a multiple of 16 only.  Each tile issues two
+// MMAs per K step that share the token operand: for gate/up the gate rows and
+// the up rows of the same 128 features (so one TMEM lane holds g and u of one
+// feature and the epilogue needs no exchange); for down two blocks of 128
+// output channels.  Two FP32 accumulators of 256 columns fill the 512 TMEM
+// columns.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: weight tiles (3-D map: K, row, expert) and token
+//               rows (2-D map, boxes of 32 rows) into a 3-stage ring;
+//   warp 1      TMEM allocation and the single MMA-issuing thread;
+//   warps 2-5   epilogue, one TMEM lane quadrant each: tcgen05.ld, SwiGLU,
+//               bf16 rounding, transpose through shared memory, coalesced
+//               16-byte stores of the token rows.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr uint32_t kATile = 128 * 128;          // 128 rows x 128 bytes
+constexpr uint32_t kBTile = kChunkMax * 128;     // 256 rows x 128 bytes
+constexpr uint32_t kBox = kBoxRows * 128;        // one TMA box of token rows
+constexpr uint32_t kStage = 2 * kATile + kBTile;  // 64 KB
+constexpr int kStgStride = 264;                   // staging row stride (bf16), 16-byte multiple
+constexpr uint32_t kStgBytes = 32 * kStgStride * 2;
+constexpr uint32_t kCtrl = 1024;
+constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
+
+enum Mode : int { kGateUp = 0, kDown = 1 };
+
+struct TileInfo {
+  int g, m, tok0, n, expert, brow0;
+  bool shared_b;
+  int out_row0;
+};
+
+__device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups, const int* __restrict__ ts,
+                                            int G, int E, int tile, int mode, TileInfo& ti) {
+  int lo = 0, hi = G;  // find g with ts[g] <= tile < ts[g+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ts + mid) <= tile) lo = mid;
+    else hi = mid;
+  }
+  const int g = lo;
+  const GroupInfo gi = groups[g];
+  if (gi.nchunks <= 0) return false;
+  const int local = tile - __ldg(ts + g);
+  ti.g = g;
+  ti.m = local / gi.nchunks;
+  const int c = local - ti.m * gi.nchunks;
+  ti.tok0 = c * gi.csize;
+  ti.n = min(gi.csize, gi.n - ti.tok0);
+  ti.expert = gi.expert;
+  ti.out_row0 = gi.out_row0 + ti.tok0;
+  ti.shared_b = (mode == kGateUp) && g >= E;
+  ti.brow0 = (mode == kGateUp ? gi.in_row0 : gi.out_row0) + ti.tok0;
+  return ti.n > 0;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
+                       const __grid_constant__ CUtensorMap map_b1, const GroupInfo* __restrict__ groups,
+                       const int* __restrict__ tile_start, int G, int E, int K, int I, int d,
+                       uint16_t* __restrict__ out, int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kStages * kStage);
+  uint8_t* ctrl = smem + kStages * kStage + kStgBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // [kStages]
+  uint64_t* empty = full + kStages;                    // [kStages]
+  uint64_t* tmem_full = empty + kStages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 132);
+  volatile int* zero_flag = reinterpret_cast<volatile int*>(ctrl + 136);
+  int* last_round = reinterpret_cast<int*>(ctrl + 144);  // [kStages]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = K / 64;
+  const int total = __ldg(tile_start + G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      last_round[s] = -1;
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *zero_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_w);
+    tma_prefetch_desc(&map_b0);
+    tma_prefetch_desc(&map_b1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        TileInfo ti;
+        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+        const int nbox = (ti.n + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = 2 * kATile + nbox * kBox;
+        int a0_row, a1_row;
+        if (MODE == kGateUp) {
+          a0_row = ti.m * 128;
+          a1_row = I + ti.m * 128;
+        } else {
+          a0_row = ti.m * 256;
+          a1_row = ti.m * 256 + 128;
+        }
+        const CUtensorMap* mb = ti.shared_b ? &map_b1 : &map_b0;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages, r = it / kStages;
+          if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStage;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_3d(st, &map_w, &full[s], kb * 64, a0_row, ti.expert);
+          tma_load_3d(st + kATile, &map_w, &full[s], kb * 64, a1_row, ti.expert);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(st + 2 * kATile + b * kBox, mb, &full[s], kb * 64, ti.brow0 + b * kBoxRows);
+          last_round[s] = r;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        TileInfo ti;
+        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+        const int nm = (ti.n + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(128, nm);
+        if (!mbar_wait(tmem_empty, (tl & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages, r = it / kStages;
+          if (!mbar_wait(&full[s], r & 1, abort_flag, status, status + 1, kSiteGemmMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * kStage);
+          const uint32_t a1 = a0 + kATile;
+          const uint32_t b = a0 + 2 * kATile;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc_k128(b + kk * 32);
+            const uint32_t acc = (kb | kk) != 0;
+            mma_bf16(tmem, sdesc_k128(a0 + kk * 32), bd, idesc, acc);
+            mma_bf16(tmem + 256, sdesc_k128(a1 + kk * 32), bd, idesc, acc);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(tmem_full);
+        ++tl;
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, zero_flag, status, status + 1, kSiteGemmTeardown, 100000000ull);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 -> TMEM lane quadrants 2,3,0,1)
+    const int q = warp & 3;
+    const int f = q * 32 + lane;            // feature (TMEM lane) within the tile
+    const int etid = threadIdx.x - 64;      // 0..127
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t tl = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      TileInfo ti;
+      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+      if (!mbar_wait(tmem_full, tl & 1, abort_flag, status, status + 1, kSiteGemmEpi)) break;
+      tc_fence_after();
+      const int nm = (ti.n + 15) & ~15;
+      for (int c0 = 0; c0 < nm; c0 += 32) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tmem + lane_base + c0, ra);
+        tmem_ld32(tmem + lane_base + 256 + c0, rb);
+        tmem_ld_wait();
+        if (MODE == kGateUp) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float g = __uint_as_float(ra[i]);
+            const float u = __uint_as_float(rb[i]);
+            const float h = siluf_(g) * u;
+            stg[i * kStgStride + f] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            stg[i * kStgStride + f] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(ra[i])));
+            stg[i * kStgStride + 128 + f] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rb[i])));
+          }
+        }
+        named_bar_sync(1, 128);
+        const int rows_here = min(32, ti.n - c0);
+        if (MODE == kGateUp) {
+          // 128 features x 2 bytes = 16 x 16-byte chunks per token row
+          const int ch = etid & 15;
+          for (int rr = etid >> 4; rr < rows_here; rr += 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStgStride + ch * 8);
+            uint16_t* dst = out + (size_t)(ti.out_row0 + c0 + rr) * I + ti.m * 128 + ch * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
+          }
+        } else {
+          // 256 channels = 32 x 16-byte chunks per token row; channels >= d are padding
+          const int ch = etid & 31;
+          const int col = ti.m * 256 + ch * 8;
+          if (col < d) {
+            for (int rr = etid >> 5; rr < rows_here; rr += 4) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStgStride + ch * 8);
+              *reinterpret_cast<uint4*>(out + (size_t)(ti.out_row0 + c0 + rr) * d + col) = v;
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+      ++tl;
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int s = 0; s < kStages; ++s)
+      if (last_round[s] >= 0)
+        mbar_wait(&full[s], last_round[s] & 1, zero_flag, status, status + 1, kSiteGemmTeardown, 100000000ull);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One block: per group token count, chunking and the prefix sums of tiles.
+__global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
+                                GroupInfo* __restrict__ groups, int* __restrict__ ts_gu, int* __restrict__ ts_dn,
+                                int* __restrict__ status) {
+  __shared__ int sg[2][512], sd[2][512];
+  __shared__ int bad;
+  const int G = E + S;
+  const int g = threadIdx.x;
+  if (g == 0) bad = 0;
+  __syncthreads();
+  int tg = 0, td = 0;
+  if (g < G) {
+    GroupInfo gi{};
+    const int Tk = T * k;
+    if (g < E) {
+      const int lo = offsets[g], hi = offsets[g + 1];
+      if (lo < 0 || hi < lo || hi > Tk || (g == E - 1 && hi != Tk) || (g == 0 && lo != 0)) {
+        bad = 1;
+        gi.n = 0;
+      } else {
+        gi.n = hi - lo;
+      }
+      gi.in_row0 = lo;
+      gi.out_row0 = lo;
+      gi.expert = g;
+    } else {
+      gi.n = T;
+      gi.in_row0 = 0;
+      gi.out_row0 = Tk + (g - E) * T;
+      gi.expert = g;
+    }
+    gi.nchunks = (gi.n + kChunkMax - 1) / kChunkMax;
+    gi.csize = gi.nchunks ? (((gi.n + gi.nchunks - 1) / gi.nchunks + 15) & ~15) : 16;
+    groups[g] = gi;
+    tg = gi.nchunks * m_gu;
+    td = gi.nchunks * m_dn;
+  }
+  // inclusive scan (Hillis-Steele) over up to 512 groups
+  int cur = 0;
+  sg[0][g] = tg;
+  sd[0][g] = td;
+  __syncthreads();
+  for (int off = 1; off < 512; off <<= 1) {
+    const int a = sg[cur][g] + (g >= off ? sg[cur][g - off] : 0);
+    const int b = sd[cur][g] + (g >= off ? sd[cur][g - off] : 0);
+    sg[cur ^ 1][g] = a;
+    sd[cur ^ 1][g] = b;
+    cur ^= 1;
+    __syncthreads();
+  }
+  if (bad) {
+    if (g == 0) set_error(status, status + 1, MOE_ERR_DEVICE, kSiteSchedule);
+    if (g <= G) {
+      ts_gu[g] = 0;
+      ts_dn[g] = 0;
+    }
+    return;
+  }
+  if (g < G) {
+    ts_gu[g + 1] = sg[cur][g];
+    ts_dn[g + 1] = sd[cur][g];
+  }
+  if (g == 0) {
+    ts_gu[0] = 0;
+    ts_dn[0] = 0;
+  }
+}
+
+}  // namespace
+
+moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
+                               const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
+                               const void* w_down, const float* w_down_scale, void* y, void* ws, cudaStream_t st) {
+  (void)x_perm_scale;
+  (void)w_gu_scale;
+  (void)w_down_scale;
+  if (s.T == 0) return MOE_OK;
+  if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(s);
+  char* w = static_cast<char*>(ws);
+  const int G = s.E + s.S;
+  GroupInfo* groups = reinterpret_cast<GroupInfo*>(w + L.sched);
+  int* ts_gu = reinterpret_cast<int*>(groups + G);
+  int* ts_dn = ts_gu + (G + 1);
+  uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
+  int* status = ws_status(ws);
+  const int Tk = s.T * s.k;
+  const int rows = Tk + s.S * s.T;
+  const int m_gu = s.I / 128;
+  const int m_dn = (s.d + 255) / 256;
+
+  schedule_kernel<<<1, 512, 0, st>>>(offsets, s.T, s.k, s.E, s.S, m_gu, m_dn, groups, ts_gu, ts_dn, status);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+
+  CUtensorMap m_wgu, m_xp, m_x, m_wd, m_h;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map_3d(&m_wgu, w_gate_up, bf, 2, s.d, 2 * (uint64_t)s.I, G, 64, 128)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_xp, x_perm, bf, 2, s.d, Tk, 64, kBoxRows)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_x, x, bf, 2, s.d, s.T, 64, kBoxRows)) return MOE_ERR_CUDA;
+  if (!make_map_3d(&m_wd, w_down, bf, 2, s.I, s.d, G, 64, 128)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_h, h, bf, 2, s.I, rows, 64, kBoxRows)) return MOE_ERR_CUDA;
+
+  const int grid = sm_count();
+  if (grid <= 0) return MOE_ERR_CUDA;
+  auto k_gu = expert_gemm_kernel<kGateUp>;
+  auto k_dn = expert_gemm_kernel<kDown>;
+  if (cudaFuncSetAttribute(k_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, groups, ts_gu, G, s.E, s.d, s.I, s.d, h, status);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d,
+                                          static_cast<uint16_t*>(y), status);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,96 @@
+// Internal declarations shared by the libmoe translation units: limits,
+// workspace layout, the expert-GEMM schedule format and host helpers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+constexpr int kMaxE = 256;
+constexpr int kMaxS = 8;
+constexpr int kMaxK = 16;
+constexpr int kRouterTileM = 128;  // tokens per router tile
+constexpr int kChunkMax = 256;     // tokens per expert-GEMM tile (tcgen05 N)
+constexpr int kBoxRows = 32;       // token rows per TMA box in the expert GEMM
+
+// Failure-site ids recorded next to the status word (diagnostics only).
+enum Site : int {
+  kSiteRouterProducer = 1,
+  kSiteRouterMma = 2,
+  kSiteRouterEpi = 3,
+  kSiteGemmProducer = 11,
+  kSiteGemmMma = 12,
+  kSiteGemmEpi = 13,
+  kSiteGemmTeardown = 14,
+  kSitePermute = 21,
+  kSiteSchedule = 22,
+  kSiteDebug = 90,
+};
+
+// Per-group record of the expert-GEMM schedule (routed experts 0..E-1, then
+// shared experts).  Written on the device by the schedule kernel.
+struct GroupInfo {
+  int n;         // tokens in the group
+  int in_row0;   // first row of the group in the gate/up B source (x_perm or x)
+  int out_row0;  // first row of the group in h / y
+  int csize;     // tokens per chunk (multiple of 16, <= kChunkMax)
+  int nchunks;   // chunks
+  int expert;    // weight index (0..E+S-1)
+  int pad0, pad1;
+};
+
+struct Schedule {
+  // layout inside the workspace: GroupInfo[G], int tile_start_gu[G+1], int tile_start_dn[G+1]
+  static size_t bytes(int G) { return sizeof(GroupInfo) * G + sizeof(int) * 2 * (G + 1); }
+};
+
+struct WsLayout {
+  size_t status, counts, offsets, idx, gate, perm_token, inv_pos, sched;
+  size_t x_perm, x_perm_scale, xq, xq_scale, h, h_scale, y;
+  size_t total;
+};
+
+bool shape_valid(const moe_shape_t* s);
+WsLayout ws_layout(const moe_shape_t& s);
+
+// status word helpers (the word lives at offset 0 of the workspace)
+inline int* ws_status(void* ws) { return reinterpret_cast<int*>(ws); }
+
+// host helpers
+moe_status_t check_ws(const moe_shape_t& s, void* ws, size_t ws_bytes);
+bool aligned16(const void* p);
+int sm_count();
+moe_status_t cuda_status(cudaError_t e);
+
+// TMA descriptors (128-byte swizzle, zero fill out of bounds)
+bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                 uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
+
+// launchers (each returns MOE_OK or MOE_ERR_CUDA); pointers already validated
+moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_router, const float* bias,
+                          const float* logit_offset, int32_t* idx, float* gate, int32_t* counts,
+                          int32_t* offsets, void* ws, cudaStream_t st);
+moe_status_t launch_permute(const moe_shape_t& s, const void* x, const int32_t* idx, const int32_t* offsets,
+                            void* x_perm, float* x_perm_scale, int32_t* perm_token, int32_t* inv_pos, void* ws,
+                            cudaStream_t st);
+moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
+                               const void* x, const int32_t* offsets, const void* w_gate_up,
+                               const float* w_gu_scale, const void* w_down, const float* w_down_scale,
+                               void* y, void* ws, cudaStream_t st);
+moe_status_t launch_combine(const moe_shape_t& s, const void* y, const float* gate, const int32_t* inv_pos,
+                            void* out, cudaStream_t st);
+moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, float* bias, float gamma,
+                                cudaStream_t st);
+moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale,
+                                  cudaStream_t st);
+moe_status_t launch_debug_wait(void* ws, unsigned limit_us, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,273 @@
+// Router: z = x . w_router^T on the tcgen05 tensor cores, fused with the
+// sigmoid affinity, the selection bias, the per-token top-k, the gate
+// normalisation over the chosen set and the per-expert load histogram.
+//
+// Pages: "deepseek-v3-report" (dynmi.github.io), load-balancing paragraph (b_i
+// added to the routing score for selection, out of the gradient);
+// "DeepSeek-V3 详解" (yudonglee.me) 2.2-2.3 (top-8 of 256, bias); readings for
+// the silent points (sigmoid, gate normalisation, tie-break) in include/moe.h.
+//
+// One CTA owns 128 tokens (the M side of the MMA, one token per TMEM lane) and
+// all E <= 256 experts (the N side, padded to 16).  Warp roles: warp 0 issues
+// TMA loads of x and w_router in 64-wide K blocks through a 4-stage ring, warp 1
+// issues tcgen05.mma into a TMEM accumulator, warps 2-5 (one per TMEM lane
+// quadrant) turn each token's row of logits into its top-k.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+
+struct RouterSmem {
+  uint32_t a_bytes, b_bytes, stage_bytes, ctrl;
+};
+
+__host__ __device__ inline RouterSmem router_smem(int E) {
+  RouterSmem r;
+  const int np = (E + 15) & ~15;
+  r.a_bytes = kRouterTileM * 128;
+  r.b_bytes = np * 128;
+  r.stage_bytes = r.a_bytes + r.b_bytes;  // multiple of 2048
+  r.ctrl = kStages * r.stage_bytes;
+  return r;
+}
+
+constexpr size_t kCtrlBytes = 4096;  // barriers, flags, bias, offsets, histogram
+
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
+                  int d, int E, int k, const float* __restrict__ bias, const float* __restrict__ logit_offset,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int32_t* __restrict__ counts,
+                  int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const RouterSmem L = router_smem(E);
+  uint8_t* ctrl = smem + L.ctrl;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);          // [kStages]
+  uint64_t* empty = full + kStages;                             // [kStages]
+  uint64_t* tmem_full = empty + kStages;
+  uint64_t* drain = tmem_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 84);
+  volatile int* zero_flag = reinterpret_cast<volatile int*>(ctrl + 88);  // stays 0
+  int* last_round = reinterpret_cast<int*>(ctrl + 96);                   // [kStages]
+  float* s_bias = reinterpret_cast<float*>(ctrl + 256);
+  float* s_off = s_bias + kMaxE;
+  int* s_hist = reinterpret_cast<int*>(s_off + kMaxE);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int nk = d / 64;
+  const int np = (E + 15) & ~15;
+  uint32_t ncols = 32;
+  while ((int)ncols < np) ncols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      last_round[s] = -1;
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *zero_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_w);
+  }
+  for (int i = threadIdx.x; i < kMaxE; i += kThreads) {
+    s_bias[i] = i < E ? bias[i] : 0.0f;
+    s_off[i] = (i < E && logit_offset) ? logit_offset[i] : 0.0f;
+    s_hist[i] = 0;
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, r = kb / kStages;
+      if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteRouterProducer)) break;
+      uint8_t* st = smem + s * L.stage_bytes;
+      mbar_arrive_expect_tx(&full[s], L.stage_bytes);
+      tma_load_2d(st, &map_x, &full[s], kb * 64, tile * kRouterTileM);
+      tma_load_2d(st + L.a_bytes, &map_w, &full[s], kb * 64, 0);
+      last_round[s] = r;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t idesc = idesc_bf16(128, np);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, r = kb / kStages;
+      if (!mbar_wait(&full[s], r & 1, abort_flag, status, status + 1, kSiteRouterMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a = smem_u32(smem + s * L.stage_bytes);
+      const uint32_t b = a + L.a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(tmem, sdesc_k128(a + kk * 32), sdesc_k128(b + kk * 32), idesc, (kb | kk) != 0);
+      mma_commit(&empty[s]);
+    }
+    if (ok) mma_commit(tmem_full);
+    // drain: every MMA of this thread has finished before TMEM is released
+    mma_commit(drain);
+    mbar_wait(drain, 0, abort_flag, status, status + 1, kSiteRouterMma, 100000000ull);
+  } else if (warp >= 2) {
+    // ---- epilogue: one token per thread
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int t = tile * kRouterTileM + row;
+    if (mbar_wait(tmem_full, 0, abort_flag, status, status + 1, kSiteRouterEpi)) {
+      tc_fence_after();
+      float tv[KMAX], ts[KMAX];
+      int ti[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        tv[j] = -INFINITY;
+        ts[j] = 0.0f;
+        ti[j] = 0;
+      }
+      float kth = -INFINITY;  // score of the k-th entry (tv[k-1])
+      for (int c0 = 0; c0 < np; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c0 + i;
+          if (e < E) {
+            const float z = __uint_as_float(r[i]) + s_off[e];
+            const float s = sigmoidf_(z);
+            float v = s + s_bias[e];
+            v = (v == v) ? fminf(fmaxf(v, -3.0e38f), 3.0e38f) : -3.0e38f;
+            if (v > kth) {
+              // insert keeping descending order; equal scores keep the earlier (lower) expert first
+#pragma unroll
+              for (int j = KMAX - 1; j >= 1; --j) {
+                if (j < k) {
+                  if (tv[j - 1] < v) {  // slot j-1 moves down
+                    tv[j] = tv[j - 1];
+                    ts[j] = ts[j - 1];
+                    ti[j] = ti[j - 1];
+                  } else if (tv[j] < v) {  // insertion point
+                    tv[j] = v;
+                    ts[j] = s;
+                    ti[j] = e;
+                  }
+                }
+              }
+              if (tv[0] < v) {
+                tv[0] = v;
+                ts[0] = s;
+                ti[0] = e;
+              }
+              kth = INFINITY;  // the list is sorted, so tv[k-1] is its minimum
+#pragma unroll
+              for (int j = 0; j < KMAX; ++j)
+                if (j < k) kth = fminf(kth, tv[j]);
+            }
+          }
+        }
+      }
+      if (t < T) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) sum += ts[j];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (j < k) {
+            topk_idx[(size_t)t * k + j] = ti[j];
+            topk_gate[(size_t)t * k + j] = __fdiv_rn(ts[j], sum);
+            atomicAdd(&s_hist[ti[j]], 1);
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    named_bar_sync(1, 128);
+    for (int e = threadIdx.x - 64; e < E; e += 128)
+      if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
+  }
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // do not leave TMA writes in flight into shared memory
+    for (int s = 0; s < kStages; ++s)
+      if (last_round[s] >= 0)
+        mbar_wait(&full[s], last_round[s] & 1, zero_flag, status, status + 1, kSiteRouterProducer,
+                  100000000ull);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+// offsets[0] = 0, offsets[i+1] = offsets[i] + counts[i]
+__global__ void offsets_kernel(const int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int E) {
+  __shared__ int buf[2][kMaxE];
+  const int i = threadIdx.x;
+  int v = i < E ? counts[i] : 0;
+  int cur = 0;
+  buf[0][i] = v;
+  __syncthreads();
+  for (int off = 1; off < kMaxE; off <<= 1) {
+    const int nv = buf[cur][i] + (i >= off ? buf[cur][i - off] : 0);
+    buf[cur ^ 1][i] = nv;
+    cur ^= 1;
+    __syncthreads();
+  }
+  if (i < E) offsets[i + 1] = buf[cur][i];
+  if (i == 0) offsets[0] = 0;
+}
+
+}  // namespace
+
+moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_router, const float* bias,
+                          const float* logit_offset, int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
+                          void* ws, cudaStream_t st) {
+  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (s.T > 0) {
+    CUtensorMap mx, mw;
+    const int np = (s.E + 15) & ~15;
+    if (!make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.d, s.T, 64, kRouterTileM)) return MOE_ERR_CUDA;
+    if (!make_map_2d(&mw, w_router, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.d, s.E, 64, np)) return MOE_ERR_CUDA;
+    const RouterSmem L = router_smem(s.E);
+    const size_t smem = 1024 + L.ctrl + kCtrlBytes;
+    const int grid = (s.T + kRouterTileM - 1) / kRouterTileM;
+    int* status = ws_status(ws);
+    if (s.k <= 8) {
+      auto kern = router_kernel<8>;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts,
+                                         status);
+    } else {
+      auto kern = router_kernel<16>;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts,
+                                         status);
+    }
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  offsets_kernel<<<1, kMaxE, 0, st>>>(counts, offsets, s.E);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -15,3 +15,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def libmoe():
+    """Builds (if stale) and loads libmoe.so."""
+    from sparse_moe_layer_12_b300 import binding, build
+
+    build.build()
+    return binding.load()

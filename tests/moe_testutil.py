@@ -1,0 +1,72 @@
+"""Helpers shared by the GPU parity tests: oracle calls on torch tensors and the
+routing comparison rule (bit-exact except at near-tied tokens, which must hold a
+valid choice)."""
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+
+
+def np64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
+
+
+def oracle_route(x, w_router, bias, k, logit_offset=None):
+    return O.route(np64(x), np64(w_router), bias.cpu().numpy(), k,
+                   None if logit_offset is None else logit_offset.cpu().numpy())
+
+
+def check_routing(ref, idx, gate, counts, offsets, E):
+    """Returns the number of near-tied tokens; asserts everything else."""
+    idx = idx.cpu().numpy()
+    gate = gate.cpu().numpy().astype(np.float64)
+    counts = counts.cpu().numpy()
+    offsets = offsets.cpu().numpy()
+    T, k = idx.shape
+    rid = ref["idx"]
+    btie, otie = ref["boundary_tie"], ref["order_tie"]
+    clean = ~(btie | otie)
+    # 1. tokens with no tie: indices equal, in order
+    bad = np.nonzero(clean & np.any(idx != rid, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} untied tokens routed differently, first {bad[:5]}: {idx[bad[:3]]} vs {rid[bad[:3]]}"
+    # 2. ties inside the chosen set only: same set
+    only_order = otie & ~btie
+    for t in np.nonzero(only_order)[0]:
+        assert set(idx[t]) == set(rid[t]), t
+    # 3. ties at the k-th place: the chosen set must be a valid top-k within 1e-5
+    v = ref["v"].astype(np.float64)
+    for t in np.nonzero(btie)[0]:
+        assert len(set(idx[t].tolist())) == k
+        kth = np.sort(v[t])[::-1][k - 1]
+        assert np.all(v[t][idx[t]] >= kth - O.NEAR_TIE), t
+        must = np.nonzero(v[t] > kth + O.NEAR_TIE)[0]
+        assert set(must.tolist()) <= set(idx[t].tolist()), t
+    # gates: unbiased affinity of the chosen expert over the chosen sum
+    s = ref["s"].astype(np.float64)
+    s_sel = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+    g_ref = s_sel / s_sel.sum(1, keepdims=True)
+    np.testing.assert_allclose(gate, g_ref, rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(gate.sum(1), 1.0, rtol=0, atol=1e-5)
+    # counts / offsets: the oracle's choice, with the GPU's valid choice at tied tokens
+    use = np.where((btie | otie)[:, None], idx, rid)
+    exp_counts = np.bincount(use.reshape(-1), minlength=E)
+    np.testing.assert_array_equal(counts, exp_counts)
+    np.testing.assert_array_equal(offsets, O.offsets_from_counts(exp_counts))
+    return int((btie | otie).sum())
+
+
+def rel_err(out, ref) -> float:
+    return O.max_rel_err(np64(out) if isinstance(out, torch.Tensor) else out, ref)
+
+
+BF16_HALF_ULP = 2.0 ** -8  # relative half-ulp of bf16 (8 significant bits)
+
+
+def out_err(out, ref) -> float:
+    """Computation error of a bf16 output against the float64 oracle, normalised by RMS(ref):
+    max over elements of (|out - ref| - 2^-8 |ref|)+ / RMS(ref).  The 2^-8 |ref| term is the
+    rounding of storing the exact value in bf16, which no bf16 output can avoid."""
+    o = np64(out) if isinstance(out, torch.Tensor) else np.asarray(out, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref * ref))
+    return float(np.max(np.maximum(np.abs(o - ref) - BF16_HALF_ULP * np.abs(ref), 0.0)) / rms)

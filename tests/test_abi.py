@@ -1,0 +1,72 @@
+"""CPU-only checks of the C ABI: the library loads, exports exactly what
+include/moe.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_layer_12_b300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(libmoe):
+    for name in _declared():
+        assert hasattr(libmoe, name), name
+    assert libmoe.moe_version().decode().startswith("libmoe")
+
+
+def test_status_strings(libmoe):
+    for code, name in B.STATUS.items():
+        assert libmoe.moe_status_string(code).decode() == name
+
+
+def test_workspace_bytes(libmoe):
+    s = B.make_shape(8192, 7168, 256, 1, 8, 2048)
+    n = B.workspace_bytes(s)
+    # x_perm + h + y dominate: (T*k*d + rows*I + rows*d) * 2 bytes
+    rows = 8192 * 8 + 8192
+    assert n >= (8192 * 8 * 7168 + rows * 2048 + rows * 7168) * 2
+    assert n < 1.01 * (8192 * 8 * 7168 + rows * 2048 + rows * 7168) * 2 + (1 << 24)
+    assert B.workspace_bytes(B.make_shape(8192, 7000, 256, 1, 8, 2048)) == 0  # d % 128
+    assert B.workspace_bytes(B.make_shape(16, 256, 4, 1, 5, 128)) == 0  # k > E
+    f8 = B.workspace_bytes(B.make_shape(8192, 7168, 256, 1, 8, 2048, fp8=True))
+    assert f8 < n
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 256, 16, 1, 2, 128), 1),      # null pointers with a valid (empty) shape
+    ((256, 200, 16, 1, 2, 128), 1),    # d % 128
+    ((256, 256, 16, 1, 0, 128), 1),    # k = 0
+    ((256, 256, 300, 1, 8, 128), 2),   # E > 256 unsupported
+    ((256, 256, 16, 9, 2, 128), 2),    # S > 8 unsupported
+    ((256, 256, 32, 1, 17, 128), 2),   # k > 16 unsupported
+])
+def test_route_rejects_before_launch(libmoe, shape, code):
+    s = B.make_shape(*shape)
+    st = libmoe.moe_route(ctypes.byref(s), None, None, None, None, None, None, None, None, None, 0, None)
+    assert st == code
+
+
+def test_alignment_and_workspace_are_checked(libmoe):
+    s = B.make_shape(256, 256, 16, 1, 2, 128)
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10002)
+    args = [p, p, None, p, p, p, p]
+    assert libmoe.moe_route(ctypes.byref(s), odd, p, p, None, p, p, p, p, p, 1 << 30, None) == 3
+    assert libmoe.moe_route(ctypes.byref(s), p, p, p, None, p, p, p, p, None, 0, None) == 4
+    assert libmoe.moe_route(ctypes.byref(s), p, p, p, None, p, p, p, p, p, 16, None) == 4
+    assert libmoe.moe_bias_update(ctypes.byref(s), p, p, ctypes.c_float(-1.0), None) == 1
+    assert libmoe.moe_quantize_weights_fp8(1, 100, 128, p, p, p, None) == 1
+    assert libmoe.moe_debug_wait_timeout(p, 0, None) == 1
+    assert len(args) == 7
