@@ -165,6 +165,27 @@ MOE_API moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const 
                          float gamma, int update_bias, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
 
+/* The expert FFN (same arguments and results as moe_expert_ffn) for callers
+ * that cannot allocate device memory -- a plugin inside a host framework that
+ * owns all device memory and offers no workspace, or a serving loop that
+ * forbids cudaMalloc after start-up.  The paper has no counterpart; this is a
+ * deployment convenience of the library.
+ *   - Scratch (status word, schedule, SwiGLU intermediate h) comes from one
+ *     64 MiB array compiled into the library, held on every GPU that loads
+ *     the library until the process exits.  Layers needing more scratch are
+ *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (T=256 at
+ *     d=7168, 256+1 experts, top-8, I=2048 needs about 39 MB).
+ *   - The first call on a device looks up the array's address; make that call
+ *     before any stream capture.
+ *   - All calls share the array; overlapping calls on the GPU race and give
+ *     wrong results.  The status word is cleared at the start of each call.
+ *   - Allocates nothing (no cudaMalloc / cudaFree). */
+MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, const void* x_perm,
+                                           const float* x_perm_scale, const void* x,
+                                           const int32_t* offsets, const void* w_gate_up,
+                                           const float* w_gu_scale, const void* w_down,
+                                           const float* w_down_scale, void* y, moe_stream_t stream);
+
 /* FP8 weight preparation ("DeepSeek-V3 详解" 4.2): quantise `w` bf16
  * [G, N, K] (N % 128 == 0, K % 128 == 0) per 128x128 block to E4M3 `w_q`
  * [G, N, K] with f32 scales `w_scale` [G, N/128, K/128] (scale = amax/448,

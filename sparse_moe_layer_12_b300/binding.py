@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # every symbol include/moe.h declares
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
-           "moe_debug_wait_timeout", "moe_status_string", "moe_version"]
+           "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static"]
 
 
 class MoEError(RuntimeError):
@@ -45,6 +45,7 @@ _SIGS = {
     "moe_route": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn_static": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [ctypes.POINTER(Shape), _P, _P, _F, _P]),
     "moe_forward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P,
@@ -172,6 +173,24 @@ def moe_expert_ffn(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(shape), _ptr(x_perm), _ptr(x_perm_scale), _ptr(x), _ptr(offsets), _ptr(w_gate_up),
         _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def moe_expert_ffn_static(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_down, w_gu_scale=None,
+                          w_down_scale=None):
+    """moe_expert_ffn without a workspace: the library's fixed scratch array is used
+    (for callers that cannot allocate device memory; one call at a time)."""
+    T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
+    wdt = _act_dtype(shape)
+    _need(x_perm, wdt, (T * k, d), "x_perm")
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
+    _need(w_down, wdt, (E + S, d, I), "w_down")
+    y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    _check("moe_expert_ffn_static", load().moe_expert_ffn_static(
+        ctypes.byref(shape), _ptr(x_perm), _ptr(x_perm_scale), _ptr(x), _ptr(offsets), _ptr(w_gate_up),
+        _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y), _stream()))
     return y
 
 
