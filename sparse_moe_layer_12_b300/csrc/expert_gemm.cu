@@ -21,9 +21,11 @@
 //   warp 0      TMA producer: weight tiles (3-D map: K, row, expert) and token
 //               rows (2-D map, boxes of 32 rows) into a 3-stage ring;
 //   warp 1      TMEM allocation and the single MMA-issuing thread;
-//   warps 2-5   epilogue, one TMEM lane quadrant each: tcgen05.ld, SwiGLU,
+//   warps 2-9   epilogue in two groups of four (one TMEM lane quadrant per
+//               warp, alternate 32-token chunks per group): tcgen05.ld, SwiGLU,
 //               bf16 rounding, transpose through shared memory, coalesced
-//               16-byte stores of the token rows.
+//               16-byte stores of the token rows.  TMEM is handed back to the
+//               MMA warp right after the last TMEM read of a tile.
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -32,13 +34,13 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kATile = 128 * 128;          // 128 rows x 128 bytes
 constexpr uint32_t kBTile = kChunkMax * 128;     // 256 rows x 128 bytes
 constexpr uint32_t kBox = kBoxRows * 128;        // one TMA box of token rows
 constexpr uint32_t kStage = 2 * kATile + kBTile;  // 64 KB
-constexpr int kStgStride = 264;                   // staging row stride (bf16), 16-byte multiple
-constexpr uint32_t kStgBytes = 32 * kStgStride * 2;
+constexpr int kStgStride = 136;                   // staging row stride (bf16), 16-byte multiple
+constexpr uint32_t kStgBytes = 2 * 32 * kStgStride * 2;  // one [32][136] tile per epilogue group
 constexpr uint32_t kCtrl = 1024;
 constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_round[s] = -1;
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 128);
+    mbar_init(tmem_empty, 256);
     mbar_init(drain, 1);
     *abort_flag = 0;
     *zero_flag = 0;
@@ -194,10 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, zero_flag, status, status + 1, kSiteGemmTeardown, 100000000ull);
     }
   } else {
-    // ---------------- epilogue (warps 2..5 -> TMEM lane quadrants 2,3,0,1)
+    // ---------------- epilogue: two groups of four warps (warps 2-5 and 6-9); warp w
+    // reads TMEM lane quadrant w % 4, group g takes the 32-token column chunks
+    // g, g + 2, g + 4, ... of every tile
     const int q = warp & 3;
-    const int f = q * 32 + lane;            // feature (TMEM lane) within the tile
-    const int etid = threadIdx.x - 64;      // 0..127
+    const int grp = (warp - 2) >> 2;
+    const int f = q * 32 + lane;            // feature (TMEM lane) within the 128-row block
+    const int etid = (threadIdx.x - 64) & 127;
+    uint16_t* sg = stg + grp * (32 * kStgStride);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tl = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -206,51 +212,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tmem_full, tl & 1, abort_flag, status, status + 1, kSiteGemmEpi)) break;
       tc_fence_after();
       const int nm = (ti.n + 15) & ~15;
-      for (int c0 = 0; c0 < nm; c0 += 32) {
+      const int nchunk = (nm + 31) / 32;
+      const int mine = nchunk > grp ? (nchunk - grp + 1) / 2 : 0;  // chunks of this group
+      if (mine == 0) {
+        tc_fence_before();
+        mbar_arrive(tmem_empty);
+      }
+      for (int ci = 0; ci < mine; ++ci) {
+        const int c0 = (grp + 2 * ci) * 32;
         uint32_t ra[32], rb[32];
         tmem_ld32(tmem + lane_base + c0, ra);
         tmem_ld32(tmem + lane_base + 256 + c0, rb);
         tmem_ld_wait();
-        if (MODE == kGateUp) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float g = __uint_as_float(ra[i]);
-            const float u = __uint_as_float(rb[i]);
-            const float h = siluf_(g) * u;
-            stg[i * kStgStride + f] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            stg[i * kStgStride + f] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(ra[i])));
-            stg[i * kStgStride + 128 + f] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(rb[i])));
-          }
+        if (ci == mine - 1) {  // this group is done with TMEM for this tile
+          tc_fence_before();
+          mbar_arrive(tmem_empty);
         }
-        named_bar_sync(1, 128);
         const int rows_here = min(32, ti.n - c0);
-        if (MODE == kGateUp) {
-          // 128 features x 2 bytes = 16 x 16-byte chunks per token row
-          const int ch = etid & 15;
-          for (int rr = etid >> 4; rr < rows_here; rr += 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStgStride + ch * 8);
-            uint16_t* dst = out + (size_t)(ti.out_row0 + c0 + rr) * I + ti.m * 128 + ch * 8;
-            *reinterpret_cast<uint4*>(dst) = v;
+#pragma unroll
+        for (int pass = 0; pass < (MODE == kGateUp ? 1 : 2); ++pass) {
+          if (MODE == kGateUp) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(ra[i]);
+              const float u = __uint_as_float(rb[i]);
+              const float h = __fdividef(g, 1.0f + __expf(-g)) * u;  // silu(g) * u
+              sg[i * kStgStride + f] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              sg[i * kStgStride + f] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(pass == 0 ? ra[i] : rb[i])));
           }
-        } else {
-          // 256 channels = 32 x 16-byte chunks per token row; channels >= d are padding
-          const int ch = etid & 31;
-          const int col = ti.m * 256 + ch * 8;
-          if (col < d) {
-            for (int rr = etid >> 5; rr < rows_here; rr += 4) {
-              const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kStgStride + ch * 8);
-              *reinterpret_cast<uint4*>(out + (size_t)(ti.out_row0 + c0 + rr) * d + col) = v;
+          named_bar_sync(1 + grp, 128);
+          // 128 features x 2 bytes = 16 x 16-byte pieces per token row
+          const int ch = etid & 15;
+          const int col = (MODE == kGateUp ? ti.m * 128 : ti.m * 256 + pass * 128) + ch * 8;
+          const int width = MODE == kGateUp ? I : d;
+          if (col < width) {
+            for (int rr = etid >> 4; rr < rows_here; rr += 8) {
+              const uint4 v = *reinterpret_cast<const uint4*>(sg + rr * kStgStride + ch * 8);
+              *reinterpret_cast<uint4*>(out + (size_t)(ti.out_row0 + c0 + rr) * width + col) = v;
             }
           }
+          named_bar_sync(1 + grp, 128);
         }
-        named_bar_sync(1, 128);
       }
-      tc_fence_before();
-      mbar_arrive(tmem_empty);
       ++tl;
     }
   }

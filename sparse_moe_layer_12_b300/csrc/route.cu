@@ -11,7 +11,8 @@
 // all E <= 256 experts (the N side, padded to 16).  Warp roles: warp 0 issues
 // TMA loads of x and w_router in 64-wide K blocks through a 4-stage ring, warp 1
 // issues tcgen05.mma into a TMEM accumulator, warps 2-5 (one per TMEM lane
-// quadrant) turn each token's row of logits into its top-k.
+// quadrant) turn the logits into affinities in shared memory; then every warp
+// takes whole tokens and selects their top-k cooperatively (8 experts a lane).
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -38,7 +39,6 @@ __host__ __device__ inline RouterSmem router_smem(int E) {
 
 constexpr size_t kCtrlBytes = 4096;  // barriers, flags, bias, offsets, histogram
 
-template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
                   int d, int E, int k, const float* __restrict__ bias, const float* __restrict__ logit_offset,
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_bias = reinterpret_cast<float*>(ctrl + 256);
   float* s_off = s_bias + kMaxE;
   int* s_hist = reinterpret_cast<int*>(s_off + kMaxE);
+  float* s_score = reinterpret_cast<float*>(smem);  // [128][np + 1], reuses the ring after the MMAs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
@@ -126,21 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(drain);
     mbar_wait(drain, 0, abort_flag, status, status + 1, kSiteRouterMma, 100000000ull);
   } else if (warp >= 2) {
-    // ---- epilogue: one token per thread
+    // ---- phase 1 (warps 2-5, one token per TMEM lane): s = sigmoid(z + o) into
+    // shared memory, [token][expert] with a padded row, reusing the drained ring
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int t = tile * kRouterTileM + row;
     if (mbar_wait(tmem_full, 0, abort_flag, status, status + 1, kSiteRouterEpi)) {
       tc_fence_after();
-      float tv[KMAX], ts[KMAX];
-      int ti[KMAX];
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        tv[j] = -INFINITY;
-        ts[j] = 0.0f;
-        ti[j] = 0;
-      }
-      float kth = -INFINITY;  // score of the k-th entry (tv[k-1])
       for (int c0 = 0; c0 < np; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
@@ -148,60 +140,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int e = c0 + i;
-          if (e < E) {
+          if (e < np) {
             const float z = __uint_as_float(r[i]) + s_off[e];
-            const float s = sigmoidf_(z);
-            float v = s + s_bias[e];
-            v = (v == v) ? fminf(fmaxf(v, -3.0e38f), 3.0e38f) : -3.0e38f;
-            if (v > kth) {
-              // insert keeping descending order; equal scores keep the earlier (lower) expert first
-#pragma unroll
-              for (int j = KMAX - 1; j >= 1; --j) {
-                if (j < k) {
-                  if (tv[j - 1] < v) {  // slot j-1 moves down
-                    tv[j] = tv[j - 1];
-                    ts[j] = ts[j - 1];
-                    ti[j] = ti[j - 1];
-                  } else if (tv[j] < v) {  // insertion point
-                    tv[j] = v;
-                    ts[j] = s;
-                    ti[j] = e;
-                  }
-                }
-              }
-              if (tv[0] < v) {
-                tv[0] = v;
-                ts[0] = s;
-                ti[0] = e;
-              }
-              kth = INFINITY;  // the list is sorted, so tv[k-1] is its minimum
-#pragma unroll
-              for (int j = 0; j < KMAX; ++j)
-                if (j < k) kth = fminf(kth, tv[j]);
-            }
-          }
-        }
-      }
-      if (t < T) {
-        float sum = 0.0f;
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j)
-          if (j < k) sum += ts[j];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-          if (j < k) {
-            topk_idx[(size_t)t * k + j] = ti[j];
-            topk_gate[(size_t)t * k + j] = __fdiv_rn(ts[j], sum);
-            atomicAdd(&s_hist[ti[j]], 1);
+            s_score[row * (np + 1) + e] = __fdividef(1.0f, 1.0f + __expf(-z));
           }
         }
       }
       tc_fence_before();
     }
-    named_bar_sync(1, 128);
-    for (int e = threadIdx.x - 64; e < E; e += 128)
-      if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
   }
+  __syncthreads();
+  if (!*abort_flag) {
+    // ---- phase 2 (all warps, one token per warp): top-k of s + b by k rounds of a
+    // warp arg-max over 8 experts per lane (expert e = lane + 32 i); ties go to the
+    // lower expert index; gates = chosen s / sum of chosen s.
+    constexpr int kPer = kMaxE / 32;
+    for (int row = warp; row < kRouterTileM; row += kThreads / 32) {
+      const int t = tile * kRouterTileM + row;
+      if (t >= T) break;
+      float v[kPer], sc[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+          sc[i] = s_score[row * (np + 1) + e];
+          const float b = sc[i] + s_bias[e];
+          v[i] = (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
+        } else {
+          sc[i] = 0.0f;
+          v[i] = -INFINITY;
+        }
+      }
+      int my_idx = 0;
+      float my_s = 0.0f, sum = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        // lane-local best (value descending, index ascending)
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int e = lane + 32 * i;
+          if (v[i] > bv) {
+            bv = v[i];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        // the owner lane retires the winner and shares its affinity
+        float ws = 0.0f;
+        if ((bi & 31) == lane) {
+#pragma unroll
+          for (int i = 0; i < kPer; ++i)
+            if (lane + 32 * i == bi) {
+              ws = sc[i];
+              v[i] = -INFINITY;
+            }
+        }
+        ws = __shfl_sync(0xffffffffu, ws, bi & 31);
+        sum += ws;
+        if (lane == j) {
+          my_idx = bi;
+          my_s = ws;
+        }
+      }
+      if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_idx;
+        topk_gate[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+        atomicAdd(&s_hist[my_idx], 1);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads)
+    if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
   __syncthreads();
   if (warp == 0 && lane == 0 && *abort_flag) {
     // do not leave TMA writes in flight into shared memory
@@ -251,19 +270,10 @@ moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_rou
     const size_t smem = 1024 + L.ctrl + kCtrlBytes;
     const int grid = (s.T + kRouterTileM - 1) / kRouterTileM;
     int* status = ws_status(ws);
-    if (s.k <= 8) {
-      auto kern = router_kernel<8>;
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts,
-                                         status);
-    } else {
-      auto kern = router_kernel<16>;
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts,
-                                         status);
-    }
+    auto kern = router_kernel;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, status);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   offsets_kernel<<<1, kMaxE, 0, st>>>(counts, offsets, s.E);
