@@ -101,14 +101,25 @@ def quantize_weight_128x128(w) -> tuple[np.ndarray, np.ndarray]:
     return q.reshape(N, K), sc
 
 
+_LUT = None
+
+
+def _decode_fast(q) -> np.ndarray:
+    """e4m3_decode through a 256-entry table of its own values (for large arrays)."""
+    global _LUT
+    if _LUT is None:
+        _LUT = e4m3_decode(np.arange(256, dtype=np.uint8))
+    return _LUT[np.asarray(q, dtype=np.uint8)]
+
+
 def dequant_act(q, sc) -> np.ndarray:
     R, C = q.shape
-    return (e4m3_decode(q).reshape(R, C // 128, 128) * np.asarray(sc, np.float64)[:, :, None]).reshape(R, C)
+    return (_decode_fast(q).reshape(R, C // 128, 128) * np.asarray(sc, np.float64)[:, :, None]).reshape(R, C)
 
 
 def dequant_weight(q, sc) -> np.ndarray:
     N, K = q.shape
-    v = e4m3_decode(q).reshape(N // 128, 128, K // 128, 128)
+    v = _decode_fast(q).reshape(N // 128, 128, K // 128, 128)
     return (v * np.asarray(sc, np.float64)[:, None, :, None]).reshape(N, K)
 
 

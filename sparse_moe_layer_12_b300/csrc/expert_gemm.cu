@@ -276,8 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace
+
 // One block: per group token count, chunking and the prefix sums of tiles.
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
+                                int chunk_max,
                                 GroupInfo* __restrict__ groups, int* __restrict__ ts_gu, int* __restrict__ ts_dn,
                                 int* __restrict__ status) {
   __shared__ int sg[2][512], sd[2][512];
@@ -307,7 +310,7 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
       gi.out_row0 = Tk + (g - E) * T;
       gi.expert = g;
     }
-    gi.nchunks = (gi.n + kChunkMax - 1) / kChunkMax;
+    gi.nchunks = (gi.n + chunk_max - 1) / chunk_max;
     gi.csize = gi.nchunks ? (((gi.n + gi.nchunks - 1) / gi.nchunks + 15) & ~15) : 16;
     groups[g] = gi;
     tg = gi.nchunks * m_gu;
@@ -344,7 +347,6 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
   }
 }
 
-}  // namespace
 
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
                                const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
@@ -353,7 +355,9 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   (void)w_gu_scale;
   (void)w_down_scale;
   if (s.T == 0) return MOE_OK;
-  if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (s.dtype == MOE_FP8_E4M3)
+    return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale, y,
+                                 ws, st);
   const WsLayout L = ws_layout(s);
   char* w = static_cast<char*>(ws);
   const int G = s.E + s.S;
@@ -367,7 +371,8 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   const int m_gu = s.I / 128;
   const int m_dn = (s.d + 255) / 256;
 
-  schedule_kernel<<<1, 512, 0, st>>>(offsets, s.T, s.k, s.E, s.S, m_gu, m_dn, groups, ts_gu, ts_dn, status);
+  schedule_kernel<<<1, 512, 0, st>>>(offsets, s.T, s.k, s.E, s.S, m_gu, m_dn, kChunkMax, groups, ts_gu, ts_dn,
+                                     status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
   CUtensorMap m_wgu, m_xp, m_x, m_wd, m_h;

@@ -85,6 +85,14 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
                                const void* x, const int32_t* offsets, const void* w_gate_up,
                                const float* w_gu_scale, const void* w_down, const float* w_down_scale,
                                void* y, void* ws, cudaStream_t st);
+moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
+                                   const void* x, const int32_t* offsets, const void* w_gate_up,
+                                   const float* w_gu_scale, const void* w_down, const float* w_down_scale,
+                                   void* y, void* ws, cudaStream_t st);
+// per-group token counts, chunking (<= chunk_max tokens) and tile prefix sums (one block of 512 threads)
+__global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
+                                int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,
+                                int* __restrict__ ts_dn, int* __restrict__ status);
 moe_status_t launch_combine(const moe_shape_t& s, const void* y, const float* gate, const int32_t* inv_pos,
                             void* out, cudaStream_t st);
 moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, float* bias, float gamma,

@@ -76,15 +76,6 @@ __global__ void __launch_bounds__(kRankThreads)
   if (tid == 0 && running != hi - lo) set_error(status, status + 1, MOE_ERR_DEVICE, kSitePermute);
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
 template <bool FP8>
 __global__ void __launch_bounds__(kScatterThreads)
     permute_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos, int T, int d, int k,
@@ -123,17 +114,8 @@ __global__ void __launch_bounds__(kScatterThreads)
       uint4 raw = make_uint4(0, 0, 0, 0);
       if (valid) raw = __ldg(xr + v);
       bf16x8_to_f32(raw, f);
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
-      uint32_t q01 = f32x2_to_e4m3x2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale));
-      uint32_t q23 = f32x2_to_e4m3x2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale));
-      uint32_t q45 = f32x2_to_e4m3x2(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale));
-      uint32_t q67 = f32x2_to_e4m3x2(__fdiv_rn(f[6], scale), __fdiv_rn(f[7], scale));
-      const uint2 q = make_uint2(q01 | (q23 << 16), q45 | (q67 << 16));
+      uint2 q;
+      const float scale = quant_tile16(f, q);
       if (valid) {
         const int tile = v >> 4;
         for (int j = 0; j < k; ++j) {

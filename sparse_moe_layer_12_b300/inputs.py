@@ -142,6 +142,40 @@ def make_experts(cfg: MoEConfig, device="cpu") -> tuple[torch.Tensor, torch.Tens
     return wgu, wd
 
 
+_ID_WGU8, _ID_WD8 = 7, 8
+
+
+def make_expert_fp8(cfg: MoEConfig, e: int, device="cpu"):
+    """FP8 weights of expert e drawn directly (not quantised from bf16): E4M3 codes of
+    N(0, 64) values (torch's float8_e4m3fn cast) and per-128x128-block scales around
+    1/(64 sqrt(fan_in)), so that code * scale ~ N(0, 1/sqrt(fan_in)).
+    Returns (wgu_q [2I, d], wgu_scale [2I/128, d/128], wd_q [d, I], wd_scale [d/128, I/128])."""
+    out = []
+    for tid, (n, k) in ((_ID_WGU8, (2 * cfg.I, cfg.d)), (_ID_WD8, (cfg.d, cfg.I))):
+        g = _gen(device, cfg.seed, tid, e)
+        q = (torch.randn(n, k, generator=g, device=device) * 64.0).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        u = torch.rand(n // 128, k // 128, generator=g, device=device)
+        sc = (0.5 + u) / (64.0 * math.sqrt(k))
+        out += [q, sc.to(torch.float32)]
+    return tuple(out)
+
+
+def make_experts_fp8(cfg: MoEConfig, device="cpu"):
+    """All E+S experts in FP8: (wgu_q [E+S, 2I, d], wgu_scale, wd_q [E+S, d, I], wd_scale)."""
+    n = cfg.E + cfg.S
+    wgu = torch.empty(n, 2 * cfg.I, cfg.d, dtype=torch.float8_e4m3fn, device=device)
+    gs = torch.empty(n, 2 * cfg.I // 128, cfg.d // 128, dtype=torch.float32, device=device)
+    wd = torch.empty(n, cfg.d, cfg.I, dtype=torch.float8_e4m3fn, device=device)
+    ds = torch.empty(n, cfg.d // 128, cfg.I // 128, dtype=torch.float32, device=device)
+    for e in range(n):
+        a, b, c, d_ = make_expert_fp8(cfg, e, device)
+        wgu[e].copy_(a)
+        gs[e].copy_(b)
+        wd[e].copy_(c)
+        ds[e].copy_(d_)
+    return wgu, gs, wd, ds
+
+
 def make_all(cfg: MoEConfig, device="cpu") -> dict:
     wgu, wd = make_experts(cfg, device)
     return dict(
