@@ -42,7 +42,22 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--set", default="", help="override workload fields, e.g. T=512,E=16 (profiling slices)")
+    p.add_argument("--only", default="", choices=["", "route"], help="time one stage alone (profiling)")
     return p.parse_args()
+
+
+def _config(args):
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    cfg = I.CONFIGS[args.config]
+    if args.set:
+        kw = {}
+        for item in args.set.split(","):
+            key, val = item.split("=")
+            kw[key] = type(getattr(cfg, key))(val)
+        cfg = cfg.with_(name=f"{cfg.name}[{args.set}]", **kw)
+    return cfg
 
 
 def _peaks():
@@ -122,8 +137,16 @@ def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_expe
             rows = xn[p["perm_token"][p["offsets"][e]:p["offsets"][e + 1]]]
         else:
             rows = xn[:n_tok]
-        t1 = time.perf_counter()
-        O.swiglu_expert(rows, a, b)
+        if cfg.fp8:  # the oracle's FP8 expert; weight quantisation is preparation, not timed
+            from oracle import fp8 as Q
+
+            gq, gs = Q.quantize_weight_128x128(a)
+            dq, ds = Q.quantize_weight_128x128(b)
+            t1 = time.perf_counter()
+            Q.fp8_swiglu_expert(rows, gq, gs, dq, ds)
+        else:
+            t1 = time.perf_counter()
+            O.swiglu_expert(rows, a, b)
         t_ffn += time.perf_counter() - t1
         flops_done += 2.0 * rows.shape[0] * 3 * cfg.d * cfg.I
     y = np.zeros((cfg.T * cfg.k + cfg.S * cfg.T, cfg.d), dtype=np.float32)
@@ -141,6 +164,31 @@ def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_expe
                    f"{t_route + t_comb + t_ffn:.1f} s measured)"),
         "seconds_measured": t_route + t_comb + t_ffn,
     }
+
+
+class _LazyExperts:
+    """Regenerates one expert's bf16 weights at a time (the oracle samples a few experts)."""
+
+    def __init__(self, cfg, dev):
+        from sparse_moe_layer_12_b300 import inputs as I
+
+        self.cfg, self.dev, self.I, self.cache = cfg, dev, I, {}
+        self.gu = _View(self, 0)
+        self.dn = _View(self, 1)
+
+    def get(self, e, which):
+        if e not in self.cache:
+            self.cache.clear()
+            self.cache[e] = self.I.make_expert(self.cfg, e, self.dev)
+        return self.cache[e][which]
+
+
+class _View:
+    def __init__(self, owner, which):
+        self.owner, self.which = owner, which
+
+    def __getitem__(self, e):
+        return self.owner.get(int(e), self.which)
 
 
 def _setup_dist():
@@ -168,30 +216,14 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = I.CONFIGS[args.config]
+    cfg = _config(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     x = I.make_x(cfg, dev)
     wr = I.make_router(cfg, dev)
     b = I.make_bias(cfg, dev)
     off = I.make_logit_offset(cfg, dev)
-    wgu, wd = (None, None)
-    wgu_l, wd_l = {}, {}
-    n = cfg.E + cfg.S
-
-    class Lazy:
-        def __init__(self, which):
-            self.which = which
-
-        def __getitem__(self, e):
-            if e not in wgu_l:
-                wgu_l.clear()
-                wd_l.clear()
-                a, bb = I.make_expert(cfg, e, dev)
-                wgu_l[e], wd_l[e] = a, bb
-            return wgu_l[e] if self.which == 0 else wd_l[e]
-
-    wgu, wd = Lazy(0), Lazy(1)
-    assert n > 0
+    lazy = _LazyExperts(cfg, dev)
+    wgu, wd = lazy.gu, lazy.dn
     for _ in range(args.warmup if args.warmup < 1 else 1):
         cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=1, n_tok=64)
     vals = []
@@ -214,21 +246,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_route_only(args):
+    """moe_route alone on the workload's x and router weight (no expert weights needed)."""
+    import torch
+
+    from sparse_moe_layer_12_b300 import binding as B
+
+    cfg = _config(args)
+    dev = torch.device("cuda", 0)
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    x, wr, b = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
+    off = I.make_logit_offset(cfg, dev)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I)
+    ws = B.alloc_workspace(s, dev)
+    for _ in range(args.warmup):
+        B.moe_route(s, x, wr, b, off, ws=ws)
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        B.moe_route(s, x, wr, b, off, ws=ws)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / args.steps
+    gb = (cfg.T * cfg.d * 2 + cfg.E * cfg.d * 2 + cfg.T * cfg.k * 8) / 1e9
+    print(json.dumps({"stage": "route", "workload": cfg.name, "ms": ms, "GB/s": gb / (ms / 1e3),
+                      "tflops": 2 * cfg.T * cfg.d * cfg.E / (ms / 1e3) / 1e12}), flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from sparse_moe_layer_12_b300 import binding as B
+    from sparse_moe_layer_12_b300 import dp
     from sparse_moe_layer_12_b300 import inputs as I
 
     world, rank, local = _setup_dist()
     dev = torch.device("cuda", local if world > 1 else 0)
-    cfg = I.CONFIGS[args.config]
+    cfg = _config(args)
     cfg_r = cfg.with_(seed=cfg.seed + rank)  # each rank its own tokens (weak scaling); same weights
     B.load()
     fp8 = cfg.fp8
     shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)
-    shape_g = B.make_shape(cfg.T * world, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)  # bias update: global load
+
+    def gpu_update(c, b, T_global, gamma):  # bias update from the global load (every rank the same)
+        B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8), c, b, gamma)
+
     x = I.make_x(cfg_r, dev)
     wr = I.make_router(cfg, dev)
     bias = I.make_bias(cfg, dev)
@@ -255,9 +320,7 @@ def run_ours(args):
         if ev is not None:
             ev[1].record(stream)
         B.moe_combine(shape, y, gate, inv, out=out)
-        if world > 1:
-            dist.all_reduce(counts)
-        B.moe_bias_update(shape_g, counts, bias, cfg.gamma)
+        dp.bias_update_global(counts, bias, cfg.T * world, cfg.gamma, gpu_update)
 
     for _ in range(args.warmup):
         step()
@@ -290,31 +353,52 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError(f"device status {B.STATUS.get(status)} after the timed region")
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies its x from
+    # pinned host memory and its output back; copies run on their own streams, double
+    # buffered, so step i's copies overlap the neighbouring steps' compute
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
-        outh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-        ch = torch.empty(cfg.E, dtype=torch.int32).pin_memory()
-        xd = torch.empty_like(x)
+        outh = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        xd = [torch.empty_like(x) for _ in range(2)]
+        outd = [torch.empty_like(out) for _ in range(2)]
         counts_d = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("x_ready", "x_free", "out_ready", "out_free")}
+        for k in ("x_free", "out_free"):
+            for e_ in ev[k]:
+                e_.record(stream)
 
-        def e2e_step():
-            xd.copy_(xh, non_blocking=True)
-            B.moe_forward(shape, xd, wr, bias, wgu, wd, logit_offset=off, w_gu_scale=wgu_s, w_down_scale=wd_s,
-                          gamma=cfg.gamma, update_bias=(world == 1), ws=ws, out=out, routing_out=False)
-            outh.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            j = i % 2
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(ev["x_free"][j])
+                xd[j].copy_(xh, non_blocking=True)
+                ev["x_ready"][j].record(s_h2d)
+            stream.wait_event(ev["x_ready"][j])
+            stream.wait_event(ev["out_free"][j])
+            _, _, _, c = B.moe_forward(shape, xd[j], wr, bias, wgu, wd, logit_offset=off, w_gu_scale=wgu_s,
+                                       w_down_scale=wd_s, gamma=cfg.gamma, update_bias=(world == 1), ws=ws,
+                                       out=outd[j], routing_out=world > 1)
+            if world > 1:
+                dp.bias_update_global(c, bias, cfg.T * world, cfg.gamma, gpu_update)
+            ev["x_free"][j].record(stream)
+            ev["out_ready"][j].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev["out_ready"][j])
+                outh[j].copy_(outd[j], non_blocking=True)
+                ev["out_free"][j].record(s_d2h)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for i in range(max(1, args.warmup)):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b_.record(stream)
+        a.record(s_h2d)
+        for i in range(args.steps):
+            e2e_step(i)
+        b_.record(s_d2h)
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b_)
         if world > 1:
@@ -322,9 +406,11 @@ def run_ours(args):
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e_ms = float(tt.item())
         e2e = {"value": world * cfg.T * args.steps / (e_ms / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
-               "ms_per_step": e_ms / args.steps}
-        del ch
+               "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": outh[0].numel() * 2,
+               "ms_per_step": e_ms / args.steps,
+               "how": "moe_forward through the C ABI; x from pinned host memory and out back to it every step, "
+                      "copies on two side streams overlapping the neighbouring steps"}
+        del counts_d
 
     if rank != 0:
         if world > 1:
@@ -364,8 +450,11 @@ def run_ours(args):
         "e2e": e2e,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(cfg, x, wr, bias, wgu if not fp8 else I.make_experts(cfg, dev)[0],
-                                                 wd if not fp8 else I.make_experts(cfg, dev)[1], off)
+        del ws, wgu, wd
+        torch.cuda.empty_cache()
+        wgu_c = _LazyExperts(cfg, dev)
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, x, wr, bias, wgu_c.gu, wgu_c.dn, off,
+                                                 n_experts=2 if fp8 else 6)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -376,6 +465,8 @@ def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only == "route":
+        run_route_only(args)
     else:
         run_ours(args)
 

@@ -8,24 +8,28 @@
 // Every routed expert is a group of rows of x_perm; every shared expert is a
 // group over all T rows of x, scheduled in the same persistent launch.
 //
-// Tile shape ("swap AB"): the MMA's M side (128 TMEM lanes) carries weight rows
-// (output features) and its N side carries up to 256 tokens of one group, so a
-// group of n tokens is padded to a multiple of 16 only.  Each tile issues two
-// MMAs per K step that share the token operand: for gate/up the gate rows and
-// the up rows of the same 128 features (so one TMEM lane holds g and u of one
-// feature and the epilogue needs no exchange); for down two blocks of 128
-// output channels.  Two FP32 accumulators of 256 columns fill the 512 TMEM
-// columns.
+// Tile shape ("swap AB"): the MMA's M side carries weight rows (output
+// features) and its N side up to 256 tokens of one group, so a group of n
+// tokens is padded to a multiple of 16 only.  Two CTAs of a cluster form a pair
+// and run M = 256 MMAs (tcgen05 cta_group::2): each CTA stages its own 128
+// weight rows and half of the token rows, so a 48 KB stage feeds as much
+// tensor work per SM as a 64 KB single-CTA stage would, and four stages fit.
+// Each K step issues two MMAs sharing the token operand: gate rows and up rows
+// of the same 256 features (the even CTA's TMEM lanes hold features 0-127, the
+// odd CTA's 128-255, so one lane holds g and u of one feature), or two
+// 256-channel blocks of W_down.  Two FP32 accumulators of 256 columns fill the
+// 512 TMEM columns of each CTA.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: weight tiles (3-D map: K, row, expert) and token
-//               rows (2-D map, boxes of 32 rows) into a 3-stage ring;
-//   warp 1      TMEM allocation and the single MMA-issuing thread;
+// Warp roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
+//   warp 0      TMA producer of this CTA's operand halves; all loads of a stage
+//               complete on the even CTA's barrier;
+//   warp 1      TMEM allocation; in the even CTA the single MMA-issuing thread,
+//               whose commits are multicast to both CTAs;
 //   warps 2-9   epilogue in two groups of four (one TMEM lane quadrant per
 //               warp, alternate 32-token chunks per group): tcgen05.ld, SwiGLU,
 //               bf16 rounding, transpose through shared memory, coalesced
 //               16-byte stores of the token rows.  TMEM is handed back to the
-//               MMA warp right after the last TMEM read of a tile.
+//               MMA thread right after the last TMEM read of a tile.
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -33,13 +37,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
-constexpr uint32_t kATile = 128 * 128;          // 128 rows x 128 bytes
-constexpr uint32_t kBTile = kChunkMax * 128;     // 256 rows x 128 bytes
-constexpr uint32_t kBox = kBoxRows * 128;        // one TMA box of token rows
-constexpr uint32_t kStage = 2 * kATile + kBTile;  // 64 KB
-constexpr int kStgStride = 136;                   // staging row stride (bf16), 16-byte multiple
+constexpr int kStages = 4;
+constexpr int kThreads = 320;                  // producer warp, MMA warp, 8 epilogue warps
+constexpr int kKStagger = 5;                   // K-block offset between consecutive feature blocks
+constexpr uint32_t kATile = 128 * 128;         // 128 weight rows x 128 bytes
+constexpr uint32_t kBTile = (kChunkMax / 2) * 128;  // this CTA's half of <= 256 token rows
+constexpr uint32_t kBox = kBoxRows * 128;      // one TMA box of token rows
+constexpr uint32_t kStage = 2 * kATile + kBTile;  // 48 KB
+constexpr int kStgStride = 136;                // staging row stride (bf16), 16-byte multiple
 constexpr uint32_t kStgBytes = 2 * 32 * kStgStride * 2;  // one [32][136] tile per epilogue group
 constexpr uint32_t kCtrl = 1024;
 constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
@@ -47,11 +52,11 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 enum Mode : int { kGateUp = 0, kDown = 1 };
 
 struct TileInfo {
-  int g, m, tok0, n, expert, brow0;
+  int g, mp, tok0, n, expert, brow0, out_row0;
   bool shared_b;
-  int out_row0;
 };
 
+// pair tile -> group, feature-block pair mp, token chunk
 __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups, const int* __restrict__ ts,
                                             int G, int E, int tile, int mode, TileInfo& ti) {
   int lo = 0, hi = G;  // find g with ts[g] <= tile < ts[g+1]
@@ -65,8 +70,8 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
   if (gi.nchunks <= 0) return false;
   const int local = tile - __ldg(ts + g);
   ti.g = g;
-  ti.m = local / gi.nchunks;
-  const int c = local - ti.m * gi.nchunks;
+  ti.mp = local / gi.nchunks;
+  const int c = local - ti.mp * gi.nchunks;
   ti.tok0 = c * gi.csize;
   ti.n = min(gi.csize, gi.n - ti.tok0);
   ti.expert = gi.expert;
@@ -77,7 +82,7 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
                        const __grid_constant__ CUtensorMap map_b1, const GroupInfo* __restrict__ groups,
                        const int* __restrict__ tile_start, int G, int E, int K, int I, int d,
@@ -86,10 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kStages * kStage);
   uint8_t* ctrl = smem + kStages * kStage + kStgBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // [kStages]
-  uint64_t* empty = full + kStages;                    // [kStages]
-  uint64_t* tmem_full = empty + kStages;
-  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // [kStages], used in the even CTA
+  uint64_t* empty = full + kStages;                    // [kStages], both CTAs
+  uint64_t* tmem_full = empty + kStages;               // both CTAs
+  uint64_t* tmem_empty = tmem_full + 1;                // even CTA: both CTAs' epilogues arrive
   uint64_t* drain = tmem_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 132);
@@ -97,6 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* last_round = reinterpret_cast<int*>(ctrl + 144);  // [kStages]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0 = the CTA that issues the MMAs
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(nclusters_x());
   const int nk = K / 64;
   const int total = __ldg(tile_start + G);
 
@@ -107,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_round[s] = -1;
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 256);
+    mbar_init(tmem_empty, 2 * 256);
     mbar_init(drain, 1);
     *abort_flag = 0;
     *zero_flag = 0;
@@ -116,31 +124,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_b0);
     tma_prefetch_desc(&map_b1);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t full_leader = map_to_rank(smem_u32(full), 0);        // full[0] of the even CTA
+  const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: this CTA's weight rows and half of the token rows
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < total && ok; tile += npairs) {
         TileInfo ti;
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
-        const int nbox = (ti.n + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = 2 * kATile + nbox * kBox;
+        const int nm = (ti.n + 15) & ~15;
+        const int half = nm / 2;  // token rows per CTA (multiple of 8)
+        const int nbox_mine = (half + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes_pair = 2 * (2 * kATile + nbox_mine * kBox);  // both CTAs (same box count)
         int a0_row, a1_row;
         if (MODE == kGateUp) {
-          a0_row = ti.m * 128;
-          a1_row = I + ti.m * 128;
+          a0_row = ti.mp * 256 + rank * 128;        // gate rows of this CTA's 128 features
+          a1_row = I + ti.mp * 256 + rank * 128;    // up rows of the same features
         } else {
-          a0_row = ti.m * 256;
-          a1_row = ti.m * 256 + 128;
+          a0_row = ti.mp * 512 + rank * 128;        // channel block 0 of the pair (256 channels)
+          a1_row = ti.mp * 512 + 256 + rank * 128;  // channel block 1
         }
         const CUtensorMap* mb = ti.shared_b ? &map_b1 : &map_b0;
+        const int brow = ti.brow0 + rank * half;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer)) {
@@ -148,25 +161,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = smem + s * kStage;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_3d(st, &map_w, &full[s], kb * 64, a0_row, ti.expert);
-          tma_load_3d(st + kATile, &map_w, &full[s], kb * 64, a1_row, ti.expert);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(st + 2 * kATile + b * kBox, mb, &full[s], kb * 64, ti.brow0 + b * kBoxRows);
+          const uint32_t fb = full_leader + s * 8;
+          const int kq = (kb + ti.mp * kKStagger) % nk;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
+          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, ti.expert);
+          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, ti.expert);
+          for (int b = 0; b < nbox_mine; ++b)
+            tma_load_2d_pair(st + 2 * kATile + b * kBox, mb, fb, kq * 64, brow + b * kBoxRows);
           last_round[s] = r;
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA only)
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < total && ok; tile += npairs) {
         TileInfo ti;
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
         const int nm = (ti.n + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(128, nm);
+        const uint32_t idesc = idesc_bf16(256, nm);
         if (!mbar_wait(tmem_empty, (tl & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
         tc_fence_after();
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -183,16 +198,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_k128(b + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
-            mma_bf16(tmem, sdesc_k128(a0 + kk * 32), bd, idesc, acc);
-            mma_bf16(tmem + 256, sdesc_k128(a1 + kk * 32), bd, idesc, acc);
+            mma_bf16_pair(tmem, sdesc_k128(a0 + kk * 32), bd, idesc, acc);
+            mma_bf16_pair(tmem + 256, sdesc_k128(a1 + kk * 32), bd, idesc, acc);
           }
-          mma_commit(&empty[s]);
+          mma_commit_pair_mc(&empty[s], 0x3);  // stage s free in both CTAs
         }
         if (!ok) break;
-        mma_commit(tmem_full);
+        mma_commit_pair_mc(tmem_full, 0x3);
         ++tl;
       }
-      mma_commit(drain);
+      mma_commit_pair(drain);
       mbar_wait(drain, 0, zero_flag, status, status + 1, kSiteGemmTeardown, 100000000ull);
     }
   } else {
@@ -201,22 +216,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // g, g + 2, g + 4, ... of every tile
     const int q = warp & 3;
     const int grp = (warp - 2) >> 2;
-    const int f = q * 32 + lane;            // feature (TMEM lane) within the 128-row block
+    const int f = q * 32 + lane;
     const int etid = (threadIdx.x - 64) & 127;
     uint16_t* sg = stg + grp * (32 * kStgStride);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tl = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = pair; tile < total; tile += npairs) {
       TileInfo ti;
       if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
       if (!mbar_wait(tmem_full, tl & 1, abort_flag, status, status + 1, kSiteGemmEpi)) break;
       tc_fence_after();
       const int nm = (ti.n + 15) & ~15;
       const int nchunk = (nm + 31) / 32;
-      const int mine = nchunk > grp ? (nchunk - grp + 1) / 2 : 0;  // chunks of this group
+      const int mine = nchunk > grp ? (nchunk - grp + 1) / 2 : 0;
       if (mine == 0) {
         tc_fence_before();
-        mbar_arrive(tmem_empty);
+        mbar_arrive_remote(tmem_empty_leader);
       }
       for (int ci = 0; ci < mine; ++ci) {
         const int c0 = (grp + 2 * ci) * 32;
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (ci == mine - 1) {  // this group is done with TMEM for this tile
           tc_fence_before();
-          mbar_arrive(tmem_empty);
+          mbar_arrive_remote(tmem_empty_leader);
         }
         const int rows_here = min(32, ti.n - c0);
 #pragma unroll
@@ -248,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1 + grp, 128);
           // 128 features x 2 bytes = 16 x 16-byte pieces per token row
           const int ch = etid & 15;
-          const int col = (MODE == kGateUp ? ti.m * 128 : ti.m * 256 + pass * 128) + ch * 8;
+          const int col = (MODE == kGateUp ? ti.mp * 256 + rank * 128 : ti.mp * 512 + pass * 256 + rank * 128) +
+                          ch * 8;
           const int width = MODE == kGateUp ? I : d;
           if (col < width) {
             for (int rr = etid >> 4; rr < rows_here; rr += 8) {
@@ -264,15 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 0 && lane == 0 && *abort_flag) {
+    // this CTA's own loads completed on the even CTA's barriers; wait there (bounded)
     for (int s = 0; s < kStages; ++s)
-      if (last_round[s] >= 0)
+      if (last_round[s] >= 0 && rank == 0)
         mbar_wait(&full[s], last_round[s] & 1, zero_flag, status, status + 1, kSiteGemmTeardown, 100000000ull);
   }
-  __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal or read it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -351,9 +369,6 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
                                const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
                                const void* w_down, const float* w_down_scale, void* y, void* ws, cudaStream_t st) {
-  (void)x_perm_scale;
-  (void)w_gu_scale;
-  (void)w_down_scale;
   if (s.T == 0) return MOE_OK;
   if (s.dtype == MOE_FP8_E4M3)
     return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale, y,
@@ -368,8 +383,8 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   int* status = ws_status(ws);
   const int Tk = s.T * s.k;
   const int rows = Tk + s.S * s.T;
-  const int m_gu = s.I / 128;
-  const int m_dn = (s.d + 255) / 256;
+  const int m_gu = (s.I + 255) / 256;  // feature-block pairs
+  const int m_dn = (s.d + 511) / 512;
 
   schedule_kernel<<<1, 512, 0, st>>>(offsets, s.T, s.k, s.E, s.S, m_gu, m_dn, kChunkMax, groups, ts_gu, ts_dn,
                                      status);
@@ -383,14 +398,14 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   if (!make_map_3d(&m_wd, w_down, bf, 2, s.I, s.d, G, 64, 128)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_h, h, bf, 2, s.I, rows, 64, kBoxRows)) return MOE_ERR_CUDA;
 
-  const int grid = sm_count();
-  if (grid <= 0) return MOE_ERR_CUDA;
   auto k_gu = expert_gemm_kernel<kGateUp>;
   auto k_dn = expert_gemm_kernel<kDown>;
   if (cudaFuncSetAttribute(k_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaFuncSetAttribute(k_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
+  const int grid = pair_grid((const void*)k_gu, kThreads, kSmemBytes);
+  if (grid <= 0) return MOE_ERR_CUDA;
   k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, groups, ts_gu, G, s.E, s.d, s.I, s.d, h, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d,

@@ -151,70 +151,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (!*abort_flag) {
-    // ---- phase 2 (all warps, one token per warp): top-k of s + b by k rounds of a
-    // warp arg-max over 8 experts per lane (expert e = lane + 32 i); ties go to the
-    // lower expert index; gates = chosen s / sum of chosen s.
+    // ---- phase 2 (all warps): top-k of s + b by k rounds of a warp arg-max over 8
+    // experts per lane (expert e = lane + 32 i); ties go to the lower expert index;
+    // gates = chosen s / sum of chosen s.  Each warp works on kTok tokens at once so
+    // that their shuffle chains overlap.
     constexpr int kPer = kMaxE / 32;
-    for (int row = warp; row < kRouterTileM; row += kThreads / 32) {
-      const int t = tile * kRouterTileM + row;
-      if (t >= T) break;
-      float v[kPer], sc[kPer];
+    constexpr int kTok = 4;
+    for (int row0 = warp * kTok; row0 < kRouterTileM; row0 += (kThreads / 32) * kTok) {
+      float v[kTok][kPer], sc[kTok][kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-          sc[i] = s_score[row * (np + 1) + e];
-          const float b = sc[i] + s_bias[e];
-          v[i] = (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
-        } else {
-          sc[i] = 0.0f;
-          v[i] = -INFINITY;
-        }
-      }
-      int my_idx = 0;
-      float my_s = 0.0f, sum = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        // lane-local best (value descending, index ascending)
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+      for (int tt = 0; tt < kTok; ++tt) {
+        const int row = row0 + tt;
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
           const int e = lane + 32 * i;
-          if (v[i] > bv) {
-            bv = v[i];
-            bi = e;
+          if (e < E) {
+            sc[tt][i] = s_score[row * (np + 1) + e];
+            const float b = sc[tt][i] + s_bias[e];
+            v[tt][i] = (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
+          } else {
+            sc[tt][i] = 0.0f;
+            v[tt][i] = -INFINITY;
           }
+        }
+      }
+      int my_idx[kTok];
+      float my_s[kTok], sum[kTok];
+#pragma unroll
+      for (int tt = 0; tt < kTok; ++tt) {
+        my_idx[tt] = 0;
+        my_s[tt] = 0.0f;
+        sum[tt] = 0.0f;
+      }
+      for (int j = 0; j < k; ++j) {
+        float bv[kTok];
+        int bi[kTok];
+#pragma unroll
+        for (int tt = 0; tt < kTok; ++tt) {  // lane-local best (value descending, index ascending)
+          bv[tt] = -INFINITY;
+          bi[tt] = 0x7fffffff;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i)
+            if (v[tt][i] > bv[tt]) {
+              bv[tt] = v[tt][i];
+              bi[tt] = lane + 32 * i;
+            }
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
+#pragma unroll
+          for (int tt = 0; tt < kTok; ++tt) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv[tt], o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi[tt], o);
+            if (ov > bv[tt] || (ov == bv[tt] && oi < bi[tt])) {
+              bv[tt] = ov;
+              bi[tt] = oi;
+            }
           }
         }
-        // the owner lane retires the winner and shares its affinity
-        float ws = 0.0f;
-        if ((bi & 31) == lane) {
 #pragma unroll
-          for (int i = 0; i < kPer; ++i)
-            if (lane + 32 * i == bi) {
-              ws = sc[i];
-              v[i] = -INFINITY;
-            }
-        }
-        ws = __shfl_sync(0xffffffffu, ws, bi & 31);
-        sum += ws;
-        if (lane == j) {
-          my_idx = bi;
-          my_s = ws;
+        for (int tt = 0; tt < kTok; ++tt) {  // the owner lane retires the winner and shares its affinity
+          float ws = 0.0f;
+          if ((bi[tt] & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+              if (lane + 32 * i == bi[tt]) {
+                ws = sc[tt][i];
+                v[tt][i] = -INFINITY;
+              }
+          }
+          ws = __shfl_sync(0xffffffffu, ws, bi[tt] & 31);
+          sum[tt] += ws;
+          if (lane == j) {
+            my_idx[tt] = bi[tt];
+            my_s[tt] = ws;
+          }
         }
       }
-      if (lane < k) {
-        topk_idx[(size_t)t * k + lane] = my_idx;
-        topk_gate[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
-        atomicAdd(&s_hist[my_idx], 1);
+#pragma unroll
+      for (int tt = 0; tt < kTok; ++tt) {
+        const int t = tile * kRouterTileM + row0 + tt;
+        if (lane < k && t < T) {
+          topk_idx[(size_t)t * k + lane] = my_idx[tt];
+          topk_gate[(size_t)t * k + lane] = __fdiv_rn(my_s[tt], sum[tt]);
+          atomicAdd(&s_hist[my_idx[tt]], 1);
+        }
       }
     }
   }
