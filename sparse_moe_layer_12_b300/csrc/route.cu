@@ -21,7 +21,7 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 512;  // 16 warps: roles in warps 0-5, all warps in the top-k phase
 
 struct RouterSmem {
   uint32_t a_bytes, b_bytes, stage_bytes, ctrl;
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
                   int d, int E, int k, const float* __restrict__ bias, const float* __restrict__ logit_offset,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int32_t* __restrict__ counts,
-                  int* __restrict__ status) {
+                  int ksplit, int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const RouterSmem L = router_smem(E);
@@ -59,11 +59,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_bias = reinterpret_cast<float*>(ctrl + 256);
   float* s_off = s_bias + kMaxE;
   int* s_hist = reinterpret_cast<int*>(s_off + kMaxE);
-  float* s_score = reinterpret_cast<float*>(smem);  // [128][np + 1], reuses the ring after the MMAs
+  float* s_z = reinterpret_cast<float*>(smem);  // [128][np + 1] logits, reuses the ring after the MMAs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int nk = d / 64;
+  const int tile = blockIdx.x / ksplit;
+  const int part = blockIdx.x - tile * ksplit;
+  const int nk_all = d / 64;
+  const int per = (nk_all + ksplit - 1) / ksplit;
+  const int kb0 = part * per;
+  const int nk = max(0, min(nk_all, kb0 + per) - kb0);  // K blocks of this CTA: [kb0, kb0 + nk)
   const int np = (E + 15) & ~15;
   uint32_t ncols = 32;
   while ((int)ncols < np) ncols <<= 1;
@@ -100,8 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteRouterProducer)) break;
       uint8_t* st = smem + s * L.stage_bytes;
       mbar_arrive_expect_tx(&full[s], L.stage_bytes);
-      tma_load_2d(st, &map_x, &full[s], kb * 64, tile * kRouterTileM);
-      tma_load_2d(st + L.a_bytes, &map_w, &full[s], kb * 64, 0);
+      tma_load_2d(st, &map_x, &full[s], (kb0 + kb) * 64, tile * kRouterTileM);
+      tma_load_2d(st + L.a_bytes, &map_w, &full[s], (kb0 + kb) * 64, 0);
       last_round[s] = r;
     }
   } else if (warp == 1 && lane == 0) {
@@ -126,9 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // drain: every MMA of this thread has finished before TMEM is released
     mma_commit(drain);
     mbar_wait(drain, 0, abort_flag, status, status + 1, kSiteRouterMma, 100000000ull);
-  } else if (warp >= 2) {
-    // ---- phase 1 (warps 2-5, one token per TMEM lane): s = sigmoid(z + o) into
-    // shared memory, [token][expert] with a padded row, reusing the drained ring
+  } else if (warp >= 2 && warp < 6) {
+    // ---- phase 1 (warps 2-5, one token per TMEM lane): this CTA's partial logits
+    // into shared memory, [token][expert] with a padded row, reusing the drained ring
     const int q = warp & 3;
     const int row = q * 32 + lane;
     if (mbar_wait(tmem_full, 0, abort_flag, status, status + 1, kSiteRouterEpi)) {
@@ -138,15 +142,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = c0 + i;
-          if (e < np) {
-            const float z = __uint_as_float(r[i]) + s_off[e];
-            s_score[row * (np + 1) + e] = __fdividef(1.0f, 1.0f + __expf(-z));
-          }
-        }
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i < np) s_z[row * (np + 1) + c0 + i] = nk > 0 ? __uint_as_float(r[i]) : 0.0f;
       }
       tc_fence_before();
+    }
+  }
+  __syncthreads();
+  // With the K range split over the two CTAs of a cluster, each CTA takes half of
+  // the tile's tokens and reads the peer's partial logits for them from the peer's
+  // shared memory; the parts are added in part order (part 0 + part 1).
+  int row_lo = 0, row_hi = kRouterTileM;
+  if (ksplit == 2) {
+    cluster_sync_all();
+    row_lo = part * (kRouterTileM / 2);
+    row_hi = row_lo + kRouterTileM / 2;
+    const uint32_t peer = static_cast<uint32_t>(1 - part);
+    for (int row = row_lo + warp; row < row_hi; row += kThreads / 32) {
+      for (int e = lane; e < E; e += 32) {
+        float* zz = s_z + row * (np + 1) + e;
+        const float pv = ld_dsmem_f32(map_to_rank(smem_u32(zz), peer));
+        *zz = part == 0 ? *zz + pv : pv + *zz;
+      }
     }
   }
   __syncthreads();
@@ -156,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // gates = chosen s / sum of chosen s.  Each warp works on kTok tokens at once so
     // that their shuffle chains overlap.
     constexpr int kPer = kMaxE / 32;
-    constexpr int kTok = 4;
-    for (int row0 = warp * kTok; row0 < kRouterTileM; row0 += (kThreads / 32) * kTok) {
+    constexpr int kTok = 2;
+    for (int row0 = row_lo + warp * kTok; row0 < row_hi; row0 += (kThreads / 32) * kTok) {
       float v[kTok][kPer], sc[kTok][kPer];
 #pragma unroll
       for (int tt = 0; tt < kTok; ++tt) {
@@ -165,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
           const int e = lane + 32 * i;
-          if (e < E) {
-            sc[tt][i] = s_score[row * (np + 1) + e];
+          if (e < E && tile * kRouterTileM + row < T) {
+            const float z = s_z[row * (np + 1) + e] + s_off[e];
+            sc[tt][i] = __fdividef(1.0f, 1.0f + __expf(-z));
             const float b = sc[tt][i] + s_bias[e];
             v[tt][i] = (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
           } else {
@@ -184,48 +202,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum[tt] = 0.0f;
       }
       for (int j = 0; j < k; ++j) {
-        float bv[kTok];
-        int bi[kTok];
 #pragma unroll
-        for (int tt = 0; tt < kTok; ++tt) {  // lane-local best (value descending, index ascending)
-          bv[tt] = -INFINITY;
-          bi[tt] = 0x7fffffff;
+        for (int tt = 0; tt < kTok; ++tt) {
+          // this lane's best remaining expert (value descending, index ascending)
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
 #pragma unroll
-          for (int i = 0; i < kPer; ++i)
-            if (v[tt][i] > bv[tt]) {
-              bv[tt] = v[tt][i];
-              bi[tt] = lane + 32 * i;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-          for (int tt = 0; tt < kTok; ++tt) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv[tt], o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi[tt], o);
-            if (ov > bv[tt] || (ov == bv[tt] && oi < bi[tt])) {
-              bv[tt] = ov;
-              bi[tt] = oi;
-            }
+          for (int i = 0; i < kPer; ++i) {
+            const bool gt = v[tt][i] > bv;
+            bv = gt ? v[tt][i] : bv;
+            bi = gt ? lane + 32 * i : bi;
           }
-        }
-#pragma unroll
-        for (int tt = 0; tt < kTok; ++tt) {  // the owner lane retires the winner and shares its affinity
+          // the warp's best value via an order-preserving integer key, then the lowest
+          // expert index among the lanes that hold it
+          const uint32_t bits = __float_as_uint(bv);
+          const uint32_t key = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+          const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+          const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0x7fffffffu));
+          // the owner lane retires the winner; its affinity is broadcast
           float ws = 0.0f;
-          if ((bi[tt] & 31) == lane) {
 #pragma unroll
-            for (int i = 0; i < kPer; ++i)
-              if (lane + 32 * i == bi[tt]) {
-                ws = sc[tt][i];
-                v[tt][i] = -INFINITY;
-              }
+          for (int i = 0; i < kPer; ++i) {
+            const bool hit = lane + 32 * i == win;
+            ws = hit ? sc[tt][i] : ws;
+            v[tt][i] = hit ? -INFINITY : v[tt][i];
           }
-          ws = __shfl_sync(0xffffffffu, ws, bi[tt] & 31);
+          ws = __shfl_sync(0xffffffffu, ws, win & 31);
           sum[tt] += ws;
-          if (lane == j) {
-            my_idx[tt] = bi[tt];
-            my_s[tt] = ws;
-          }
+          my_idx[tt] = lane == j ? win : my_idx[tt];
+          my_s[tt] = lane == j ? ws : my_s[tt];
         }
       }
 #pragma unroll
@@ -242,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads)
     if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
+  if (ksplit == 2) cluster_sync_all();  // the peer has finished reading this CTA's shared memory
   __syncthreads();
   if (warp == 0 && lane == 0 && *abort_flag) {
     // do not leave TMA writes in flight into shared memory
@@ -283,18 +289,34 @@ moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_rou
                           void* ws, cudaStream_t st) {
   if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (s.T > 0) {
+    const int ntiles = (s.T + kRouterTileM - 1) / kRouterTileM;
+    // split K over the two CTAs of a cluster when that still fits one wave (1 CTA per SM)
+    const int ksplit = (2 * ntiles <= sm_count() && s.d >= 256) ? 2 : 1;
     CUtensorMap mx, mw;
     const int np = (s.E + 15) & ~15;
     if (!make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.d, s.T, 64, kRouterTileM)) return MOE_ERR_CUDA;
     if (!make_map_2d(&mw, w_router, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.d, s.E, 64, np)) return MOE_ERR_CUDA;
     const RouterSmem L = router_smem(s.E);
     const size_t smem = 1024 + L.ctrl + kCtrlBytes;
-    const int grid = (s.T + kRouterTileM - 1) / kRouterTileM;
     int* status = ws_status(ws);
     auto kern = router_kernel;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
-    kern<<<grid, kThreads, smem, st>>>(mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ntiles * ksplit), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(ksplit);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, ksplit,
+                           status) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   offsets_kernel<<<1, kMaxE, 0, st>>>(counts, offsets, s.E);
