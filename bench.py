@@ -191,6 +191,23 @@ class _View:
         return self.owner.get(int(e), self.which)
 
 
+def _traffic(fp8: bool):
+    """DRAM bytes per launch of the expert-FFN kernels, from the ncu capture recorded in
+    profiles/expert_ffn_traffic.json -- None when the kernel sources changed since."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "expert_ffn_traffic.json")) as f:
+            rec = json.load(f)["fp8" if fp8 else "bf16"]
+        h = hashlib.sha256()
+        for name in rec["sources"]:
+            with open(os.path.join(ROOT, "sparse_moe_layer_12_b300", "csrc", name), "rb") as fh:
+                h.update(fh.read())
+        return rec["bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def _setup_dist():
     import torch
     import torch.distributed as dist
@@ -258,7 +275,7 @@ def run_route_only(args):
 
     x, wr, b = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
     off = I.make_logit_offset(cfg, dev)
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, False, cfg.n_group, cfg.topk_group)
     ws = B.alloc_workspace(s, dev)
     for _ in range(args.warmup):
         B.moe_route(s, x, wr, b, off, ws=ws)
@@ -289,10 +306,10 @@ def run_ours(args):
     cfg_r = cfg.with_(seed=cfg.seed + rank)  # each rank its own tokens (weak scaling); same weights
     B.load()
     fp8 = cfg.fp8
-    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group)
 
     def gpu_update(c, b, T_global, gamma):  # bias update from the global load (every rank the same)
-        B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8), c, b, gamma)
+        B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group), c, b, gamma)
 
     x = I.make_x(cfg_r, dev)
     wr = I.make_router(cfg, dev)
@@ -443,7 +460,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "kernel": "moe_expert_ffn (grouped gate/up+SwiGLU and down GEMMs)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
-                     "traffic": None},
+                     "traffic": _traffic(fp8)},
         "stage_ms": {"expert_ffn": statistics.mean(ffn_ms), "rest": ms / args.steps - statistics.mean(ffn_ms)},
         "gpu_launches": 9 * args.steps,
         "clocks": ck,

@@ -66,10 +66,18 @@ typedef enum {
 typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_dtype_t;
 
 /* T tokens, d model width, E routed experts, S shared experts, k experts
- * chosen per token, I expert intermediate size; dtype of the expert GEMMs. */
+ * chosen per token, I expert intermediate size; dtype of the expert GEMMs.
+ * n_group, topk_group: group-limited routing ("DeepSeek-V3 技术报告要点" section 9
+ * table; "DeepSeek-V3 详解" 2.4, experts of a token on at most M nodes): the E
+ * experts form n_group contiguous groups, a group's score is the FP32 sum of its
+ * ceil(k/topk_group) largest biased scores (descending), only the topk_group best
+ * groups (ties to the lower group) are eligible for the top-k.  0, 0 = no groups.
+ * Limits: E % n_group == 0, n_group <= 32, 1 <= topk_group <= n_group,
+ * k <= topk_group * E/n_group, ceil(k/topk_group) <= E/n_group. */
 typedef struct {
   int T, d, E, S, k, I;
   moe_dtype_t dtype;
+  int n_group, topk_group;
 } moe_shape_t;
 
 /* A CUDA stream (same type as cudaStream_t). */

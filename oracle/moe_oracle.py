@@ -72,7 +72,38 @@ def affinity(z) -> np.ndarray:
     return one / (one + np.exp(-z))
 
 
-def route(x, w_router, bias, k, logit_offset=None) -> dict:
+def group_limit(v, n_group, topk_group, k):
+    """Group-limited selection ("DeepSeek-V3 技术报告要点" section 9 table: n_group /
+    topk_group; "DeepSeek-V3 详解" 2.4: a token's experts come from at most M nodes).
+
+    Reading (the pages give no group score): experts form n_group contiguous groups;
+    a group's score is the float32 sum, in descending order, of its ceil(k/topk_group)
+    largest biased scores; the topk_group best groups are kept (ties to the lower group
+    index) and every expert outside them gets -inf.  Returns (masked v, group_tie)
+    where group_tie flags tokens whose kept/dropped group scores lie within NEAR_TIE.
+    """
+    v = np.asarray(v, dtype=np.float32)
+    T, E = v.shape
+    gsz = E // n_group
+    m = -(-k // topk_group)
+    vg = v.reshape(T, n_group, gsz)
+    top_m = -np.sort(-vg, axis=2)[:, :, :m]
+    gscore = np.zeros((T, n_group), dtype=np.float32)
+    for j in range(m):
+        gscore = (gscore + top_m[:, :, j]).astype(np.float32)
+    gorder = np.argsort(-gscore, axis=1, kind="stable")
+    keep = np.zeros((T, n_group), dtype=bool)
+    np.put_along_axis(keep, gorder[:, :topk_group], True, axis=1)
+    masked = np.where(np.repeat(keep, gsz, axis=1), v, np.float32(-np.inf)).astype(np.float32)
+    if topk_group < n_group:
+        gs = np.take_along_axis(gscore, gorder, axis=1).astype(np.float64)
+        group_tie = (gs[:, topk_group - 1] - gs[:, topk_group]) < NEAR_TIE
+    else:
+        group_tie = np.zeros(T, dtype=bool)
+    return masked, group_tie
+
+
+def route(x, w_router, bias, k, logit_offset=None, n_group=0, topk_group=0) -> dict:
     """Biased top-k selection and unbiased normalised gates ([DYN], [KC], [YDL] 2.3).
 
     Returns a dict with
@@ -86,6 +117,9 @@ def route(x, w_router, bias, k, logit_offset=None) -> dict:
     s = affinity(z)
     v = s + np.asarray(bias, dtype=np.float32)[None, :]
     T, E = v.shape
+    group_tie = np.zeros(T, dtype=bool)
+    if n_group:
+        v, group_tie = group_limit(v, n_group, topk_group, k)
     # stable sort of -v: equal scores keep ascending expert order
     order = np.argsort(-v, axis=1, kind="stable")
     idx = order[:, :k].astype(np.int32)
@@ -100,7 +134,8 @@ def route(x, w_router, bias, k, logit_offset=None) -> dict:
         order_tie = (np.diff(-v_sorted[:, :k], axis=1) < NEAR_TIE).any(axis=1)
     else:
         order_tie = np.zeros(T, dtype=bool)
-    return dict(idx=idx, gate=gate, s=s, v=v, z=z, boundary_tie=boundary_tie, order_tie=order_tie)
+    return dict(idx=idx, gate=gate, s=s, v=v, z=z, boundary_tie=boundary_tie | group_tie, order_tie=order_tie,
+                group_tie=group_tie)
 
 
 def expert_counts(idx, E) -> np.ndarray:

@@ -33,7 +33,8 @@ class MoEError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("E", ctypes.c_int), ("S", ctypes.c_int),
-                ("k", ctypes.c_int), ("I", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("k", ctypes.c_int), ("I", ctypes.c_int), ("dtype", ctypes.c_int), ("n_group", ctypes.c_int),
+                ("topk_group", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -99,8 +100,8 @@ def _need(t: torch.Tensor, dtype, shape, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def make_shape(T, d, E, S, k, I, fp8=False) -> Shape:
-    return Shape(T, d, E, S, k, I, MOE_FP8_E4M3 if fp8 else MOE_BF16)
+def make_shape(T, d, E, S, k, I, fp8=False, n_group=0, topk_group=0) -> Shape:
+    return Shape(T, d, E, S, k, I, MOE_FP8_E4M3 if fp8 else MOE_BF16, n_group, topk_group)
 
 
 def workspace_bytes(shape: Shape) -> int:

@@ -19,6 +19,11 @@ bool shape_valid(const moe_shape_t* s) {
   if (s->d % 128 || s->I % 128 || s->d > 65536 || s->I > 65536) return false;
   if (s->k > s->E) return false;
   if (s->dtype != MOE_BF16 && s->dtype != MOE_FP8_E4M3) return false;
+  if (s->n_group == 0) return s->topk_group == 0;
+  if (s->n_group < 1 || s->n_group > 32 || s->E % s->n_group) return false;
+  if (s->topk_group < 1 || s->topk_group > s->n_group) return false;
+  const int gsz = s->E / s->n_group;
+  if (s->k > s->topk_group * gsz || (s->k + s->topk_group - 1) / s->topk_group > gsz) return false;
   return true;
 }
 

@@ -39,11 +39,66 @@ __host__ __device__ inline RouterSmem router_smem(int E) {
 
 constexpr size_t kCtrlBytes = 4096;  // barriers, flags, bias, offsets, histogram
 
+__device__ __forceinline__ uint32_t order_key(float v) {  // monotone float -> uint32
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Group-limited selection for one token held by a warp (expert e = lane + 32 i):
+// group score = FP32 sum, in descending order, of the group's ceil(k / topk_group)
+// largest biased scores; the topk_group best groups (ties to the lower group) stay
+// eligible, every other expert's score becomes -inf.
+__device__ __forceinline__ void group_limit(float (&v)[kMaxE / 32], int lane, int E, int k, int n_group,
+                                            int topk_group) {
+  constexpr int kPer = kMaxE / 32;
+  const int gsz = E / n_group;
+  const int m = (k + topk_group - 1) / topk_group;
+  float gs_lane = -INFINITY;  // lane g holds the score of group g
+  for (int g = 0; g < n_group; ++g) {
+    uint32_t taken = 0;
+    float sum = 0.0f;
+    for (int r = 0; r < m; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        const bool ok = e < E && e / gsz == g && !((taken >> i) & 1u) && v[i] > bv;
+        bv = ok ? v[i] : bv;
+        bi = ok ? e : bi;
+      }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(bv));
+      const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, order_key(bv) == kmax ? (uint32_t)bi : 0x7fffffffu));
+      sum += key_value(kmax);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (lane + 32 * i == win) taken |= 1u << i;
+    }
+    gs_lane = lane == g ? sum : gs_lane;
+  }
+  uint32_t keep = 0;
+  float gv = lane < n_group ? gs_lane : -INFINITY;
+  for (int r = 0; r < topk_group; ++r) {
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(gv));
+    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, order_key(gv) == kmax ? (uint32_t)lane : 32u));
+    keep |= 1u << win;
+    gv = lane == win ? -INFINITY : gv;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && !((keep >> (e / gsz)) & 1u)) v[i] = -INFINITY;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
                   int d, int E, int k, const float* __restrict__ bias, const float* __restrict__ logit_offset,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int32_t* __restrict__ counts,
-                  int ksplit, int* __restrict__ status) {
+                  int ksplit, int n_group, int topk_group, int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const RouterSmem L = router_smem(E);
@@ -193,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (n_group > 0) {
+#pragma unroll
+        for (int tt = 0; tt < kTok; ++tt) group_limit(v[tt], lane, E, k, n_group, topk_group);
+      }
       int my_idx[kTok];
       float my_s[kTok], sum[kTok];
 #pragma unroll
@@ -315,7 +374,7 @@ moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_rou
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, ksplit,
-                           status) != cudaSuccess)
+                           s.n_group, s.topk_group, status) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }

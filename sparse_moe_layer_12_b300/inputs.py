@@ -37,6 +37,8 @@ class MoEConfig:
     bias_uniform: float = 0.0  # b ~ U(-a, a); 0 -> b = 0
     zipf_amp: float = 0.0  # logit offsets A * r^-1.1; 0 -> none
     fp8: bool = False
+    n_group: int = 0  # group-limited routing: groups of experts (0 = none)
+    topk_group: int = 0  # groups kept per token
     seed: int = 0
     gamma: float = 0.001
 
@@ -65,6 +67,8 @@ CONFIGS: dict[str, MoEConfig] = {
     "v3": MoEConfig("v3", 8192, 7168, 256, 1, 8, 2048, 0.006),
     # V3-shaped FP8 path: T=16384
     "v3fp8": MoEConfig("v3fp8", 16384, 7168, 256, 1, 8, 2048, 0.006, fp8=True),
+    # V3 shape with group-limited routing: 8 groups of 32 experts, 4 groups per token
+    "v3grp": MoEConfig("v3grp", 8192, 7168, 256, 1, 8, 2048, 0.006, n_group=8, topk_group=4),
     # skewed-load decode regime: T=256 with Zipf(1.1) logit offsets, amplitude 2.0
     "skew": MoEConfig("skew", 256, 7168, 256, 1, 8, 2048, 0.006, zipf_amp=2.0),
 }

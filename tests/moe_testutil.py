@@ -11,12 +11,13 @@ def np64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().double().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
 
 
-def oracle_route(x, w_router, bias, k, logit_offset=None):
+def oracle_route(x, w_router, bias, k, logit_offset=None, n_group=0, topk_group=0):
     return O.route(np64(x), np64(w_router), bias.cpu().numpy(), k,
-                   None if logit_offset is None else logit_offset.cpu().numpy())
+                   None if logit_offset is None else logit_offset.cpu().numpy(), n_group=n_group,
+                   topk_group=topk_group)
 
 
-def check_routing(ref, idx, gate, counts, offsets, E):
+def check_routing(ref, idx, gate, counts, offsets, E, n_group=0, topk_group=0):
     """Returns the number of near-tied tokens; asserts everything else."""
     idx = idx.cpu().numpy()
     gate = gate.cpu().numpy().astype(np.float64)
@@ -35,7 +36,12 @@ def check_routing(ref, idx, gate, counts, offsets, E):
         assert set(idx[t]) == set(rid[t]), t
     # 3. ties at the k-th place: the chosen set must be a valid top-k within 1e-5
     v = ref["v"].astype(np.float64)
-    for t in np.nonzero(btie)[0]:
+    gtie = ref.get("group_tie", np.zeros(T, dtype=bool))
+    if n_group:
+        gsz = E // n_group
+        for t in range(T):
+            assert len({e // gsz for e in idx[t].tolist()}) <= topk_group, t
+    for t in np.nonzero(btie & ~gtie)[0]:
         assert len(set(idx[t].tolist())) == k
         kth = np.sort(v[t])[::-1][k - 1]
         assert np.all(v[t][idx[t]] >= kth - O.NEAR_TIE), t

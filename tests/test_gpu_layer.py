@@ -199,3 +199,20 @@ def test_debug_wait_times_out(libmoe):
     B.moe_debug_wait_timeout(ws, 2000)
     assert B.moe_get_device_status(ws) == 6  # MOE_ERR_TIMEOUT
     assert B.moe_get_device_status(ws) == 0
+
+
+def test_forward_group_limited(libmoe):
+    cfg = I.CONFIGS["tiny"].with_(n_group=4, topk_group=2, k=3, seed=5)
+    x = I.make_x(cfg, DEV)
+    wr = I.make_router(cfg, DEV)
+    b = I.make_bias(cfg, DEV)
+    wgu, wd = I.make_experts(cfg, DEV)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, n_group=4, topk_group=2)
+    out, idx, gate, counts = B.moe_forward(s, x, wr, b.clone(), wgu, wd)
+    torch.cuda.synchronize()
+    ref = oracle_route(x, wr, b, cfg.k, None, 4, 2)
+    offsets = torch.tensor(O.offsets_from_counts(counts.cpu().numpy()))
+    check_routing(ref, idx, gate, counts, offsets, cfg.E, 4, 2)
+    clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
+    yr = O.forward_rows(clean, np64(x), ref, lambda e: (np64(wgu[e]), np64(wd[e])), cfg.E, cfg.S)
+    assert out_err(np64(out)[clean], yr) < TOL_BF16

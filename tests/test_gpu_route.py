@@ -23,12 +23,12 @@ def _route_case(cfg, logit_offset=None, bias=None):
     x = I.make_x(cfg, DEV)
     wr = I.make_router(cfg, DEV)
     b = I.make_bias(cfg, DEV) if bias is None else bias
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, n_group=cfg.n_group, topk_group=cfg.topk_group)
     idx, gate, counts, offsets = B.moe_route(s, x, wr, b, logit_offset)
     ws = B.alloc_workspace(s)
     torch.cuda.synchronize()
-    ref = oracle_route(x, wr, b, cfg.k, logit_offset)
-    ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
+    ref = oracle_route(x, wr, b, cfg.k, logit_offset, cfg.n_group, cfg.topk_group)
+    ties = check_routing(ref, idx, gate, counts, offsets, cfg.E, cfg.n_group, cfg.topk_group)
     # deterministic run to run
     idx2, gate2, counts2, offsets2 = B.moe_route(s, x, wr, b, logit_offset, ws=ws)
     assert torch.equal(idx, idx2) and torch.equal(gate, gate2) and torch.equal(counts, counts2)
@@ -36,7 +36,7 @@ def _route_case(cfg, logit_offset=None, bias=None):
     return ties
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid", "v3"])
+@pytest.mark.parametrize("name", ["tiny", "mid", "v3", "v3grp"])
 def test_route_configs(libmoe, name):
     ties = _route_case(I.CONFIGS[name])
     print(f"{name}: near-tied tokens {ties}")
@@ -52,6 +52,13 @@ def test_route_skew_offsets(libmoe):
                                      (129, 128, 256, 8), (77, 640, 5, 5)])
 def test_route_ragged(libmoe, T, d, E, k):
     cfg = I.MoEConfig("rag", T, d, E, 1, k, 128, 0.05, bias_uniform=0.1, seed=T + E)
+    _route_case(cfg)
+
+
+@pytest.mark.parametrize("T,d,E,k,ng,tg", [(500, 256, 64, 6, 8, 3), (130, 384, 256, 8, 8, 4), (77, 128, 32, 4, 4, 1),
+                                           (300, 256, 16, 4, 4, 4)])
+def test_route_group_limited(libmoe, T, d, E, k, ng, tg):
+    cfg = I.MoEConfig("grp", T, d, E, 1, k, 128, 0.05, bias_uniform=0.1, seed=T + E, n_group=ng, topk_group=tg)
     _route_case(cfg)
 
 

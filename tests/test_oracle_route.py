@@ -196,3 +196,60 @@ def test_max_rel_err_definition():
     ref = np.array([3.0, -4.0])  # RMS = sqrt(12.5)
     out = np.array([3.5, -4.0])
     assert abs(O.max_rel_err(out, ref) - 0.5 / np.sqrt(12.5)) < 1e-15
+
+
+def _brute_grouped(v, n_group, topk_group, k):
+    """All group subsets of size topk_group; the best by group score, then the best
+    k-subset of the experts in the kept groups (by the sum of biased scores)."""
+    E = v.shape[0]
+    gsz = E // n_group
+    m = -(-k // topk_group)
+    gscore = []
+    for g in range(n_group):
+        top = sorted(v[g * gsz:(g + 1) * gsz].tolist(), reverse=True)[:m]
+        acc = np.float32(0)
+        for t in top:
+            acc = np.float32(acc + np.float32(t))
+        gscore.append(float(acc))
+    best_groups = max(itertools.combinations(range(n_group), topk_group), key=lambda c: sum(gscore[g] for g in c))
+    allowed = [e for g in best_groups for e in range(g * gsz, (g + 1) * gsz)]
+    return set(max(itertools.combinations(allowed, k), key=lambda c: sum(float(v[e]) for e in c)))
+
+
+@pytest.mark.parametrize("E,n_group,topk_group,k", [(12, 4, 2, 3), (12, 3, 1, 2), (16, 4, 2, 4), (8, 2, 2, 3)])
+def test_group_limited_topk_brute_force(E, n_group, topk_group, k):
+    rng = np.random.default_rng(E + 7 * n_group + k)
+    T, d = 30, 16
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    w = (rng.standard_normal((E, d)) * 0.4).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    r = O.route(x, w, b, k, n_group=n_group, topk_group=topk_group)
+    s_v = O.route(x, w, b, k)["v"]  # unmasked biased scores
+    gsz = E // n_group
+    for t in range(T):
+        assert set(r["idx"][t].tolist()) == _brute_grouped(s_v[t], n_group, topk_group, k)
+        assert len({e // gsz for e in r["idx"][t].tolist()}) <= topk_group
+
+
+def test_group_limit_all_groups_is_plain_topk():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((50, 8)).astype(np.float32)
+    w = rng.standard_normal((16, 8)).astype(np.float32)
+    b = np.zeros(16, np.float32)
+    a = O.route(x, w, b, 4)
+    g = O.route(x, w, b, 4, n_group=4, topk_group=4)
+    np.testing.assert_array_equal(a["idx"], g["idx"])
+    np.testing.assert_array_equal(a["gate"], g["gate"])
+
+
+def test_group_limit_changes_selection_by_hand():
+    # 4 experts in 2 groups of 2, top-2 from 1 group: scores (bias only, z = 0 -> s = 0.5)
+    # group 0 = {0.9, 0.0}, group 1 = {0.8, 0.7}; group scores with m = 2: 0.9 vs 1.5
+    x = np.ones((1, 1), np.float32)
+    w = np.zeros((4, 1), np.float32)
+    b = np.array([0.4, -0.5, 0.3, 0.2], np.float32)  # v = s + b = 0.9, 0.0, 0.8, 0.7
+    plain = O.route(x, w, b, 2)
+    np.testing.assert_array_equal(plain["idx"][0], [0, 2])
+    grp = O.route(x, w, b, 2, n_group=2, topk_group=1)
+    np.testing.assert_array_equal(grp["idx"][0], [2, 3])
+    np.testing.assert_allclose(grp["gate"][0], [0.5, 0.5])  # unbiased s are all 0.5
