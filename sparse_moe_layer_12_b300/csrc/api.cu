@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "moe_device.cuh"
@@ -171,6 +173,14 @@ moe_status_t launch_debug_wait(void* ws, unsigned limit_us, cudaStream_t st) {
 
 using namespace moe;
 
+namespace {
+// NVTX range around each entry point (no cost unless a profiler is attached)
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+
 #define MOE_TRY(expr)                     \
   do {                                    \
     moe_status_t _st = (expr);            \
@@ -193,6 +203,7 @@ static moe_status_t validate_shape(const moe_shape_t* shape) {
 moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_router, const float* bias,
                        const float* logit_offset, int32_t* topk_idx, float* topk_gate, int32_t* counts,
                        int32_t* offsets, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_route");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!x || !w_router || !bias || !topk_idx || !topk_gate || !counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -205,6 +216,7 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_ro
 moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t* topk_idx,
                          const int32_t* offsets, void* x_perm, float* x_perm_scale, int32_t* perm_token,
                          int32_t* inv_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_permute");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!x || !topk_idx || !offsets || !x_perm || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
@@ -219,6 +231,7 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const 
                             const void* x, const int32_t* offsets, const void* w_gate_up,
                             const float* w_gu_scale, const void* w_down, const float* w_down_scale, void* y,
                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_expert_ffn");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!x_perm || !x || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
@@ -232,6 +245,7 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const 
 
 moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* topk_gate,
                          const int32_t* inv_pos, void* out, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_combine");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!y || !topk_gate || !inv_pos || !out) return MOE_ERR_INVALID_ARG;
@@ -241,6 +255,7 @@ moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* t
 
 moe_status_t moe_bias_update(const moe_shape_t* shape, const int32_t* counts, float* bias, float gamma,
                              moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_bias_update");
   MOE_TRY(validate_shape(shape));
   if (!counts || !bias) return MOE_ERR_INVALID_ARG;
   if (!(gamma >= 0.0f) || gamma > 1.0f) return MOE_ERR_INVALID_ARG;
@@ -252,6 +267,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
                          const void* w_down, const float* w_down_scale, void* out, int32_t* topk_idx,
                          float* topk_gate, int32_t* counts, float gamma, int update_bias, void* ws,
                          size_t ws_bytes, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_forward");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!x || !w_router || !bias || !w_gate_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
@@ -282,6 +298,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
 
 moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q, float* w_scale,
                                       moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_quantize_weights_fp8");
   if (G < 0 || N < 0 || K < 0 || N % 128 || K % 128) return MOE_ERR_INVALID_ARG;
   if ((long long)G * N * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
   if (G == 0 || N == 0 || K == 0) return MOE_OK;
