@@ -328,12 +328,25 @@ def run_ours(args):
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
+    y_buf = torch.empty(cfg.rows_total, cfg.d, dtype=torch.bfloat16, device=dev)
+    gathers = B.forward_gathers(shape)
+    act_dtype = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    xp_buf = None if gathers else torch.empty(cfg.rows_routed, cfg.d, dtype=act_dtype, device=dev)
+    xps_buf = (torch.empty(cfg.rows_routed, cfg.d // 128, dtype=torch.float32, device=dev)
+               if fp8 and not gathers else None)
+
     def step(ev=None):
+        # the layer as moe_forward runs it, through its separate calls so that the
+        # expert FFN can be timed on its own; the dispatch form is moe_forward's
         idx, gate, counts, offsets = B.moe_route(shape, x, wr, bias, off, ws=ws)
-        xp, xps, ptok, inv = B.moe_permute(shape, x, idx, offsets, ws=ws)
+        xp, xps, ptok, inv = B.moe_permute(shape, x, idx, offsets, ws=ws, rows=not gathers, x_perm=xp_buf,
+                                           x_perm_scale=xps_buf)
         if ev is not None:
             ev[0].record(stream)
-        y = B.moe_expert_ffn(shape, xp, xps, x, offsets, wgu, wd, wgu_s, wd_s, ws=ws)
+        if gathers:
+            y = B.moe_expert_ffn_gather(shape, x, ptok, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
+        else:
+            y = B.moe_expert_ffn(shape, xp, xps, x, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
         if ev is not None:
             ev[1].record(stream)
         B.moe_combine(shape, y, gate, inv, out=out)
@@ -503,7 +516,10 @@ def run_ours(args):
         "timing": {"eager_ms_per_step": eager_ms / args.steps,
                    "graph_ms_per_step": None if graph_ms is None else graph_ms / args.steps,
                    "value_from": "graph replay" if ms != eager_ms else "eager launches"},
-        "gpu_launches": 9 * args.steps,
+        # per step: router, offsets, permute tables, [permuted copy,] schedule, [E4M3 copy of x,]
+        # gate/up, down, combine, bias update
+        "gpu_launches": (8 + (0 if gathers else 1) + (1 if fp8 and (gathers or cfg.S > 0) else 0)) * args.steps,
+        "dispatch": "rows gathered from x inside the gate/up GEMM" if gathers else "permuted copy + tile loads",
         "clocks": ck,
         "e2e": e2e,
     }

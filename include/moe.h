@@ -121,7 +121,9 @@ MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const vo
  *   perm_token   int32 [T*k]   out    token of each permuted row
  *   inv_pos      int32 [T, k]  out    permuted row of (t, j)
  * FP8 quantisation (scale = amax/448 per 1x128 tile, RNE, saturating) is
- * done on the way.  Inconsistent idx/offsets set MOE_ERR_DEVICE. */
+ * done on the way.  Inconsistent idx/offsets set MOE_ERR_DEVICE.
+ * x_perm = NULL (and x_perm_scale = NULL): only perm_token and inv_pos are
+ * built, no row is copied -- the input of moe_expert_ffn_gather. */
 MOE_API moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t* topk_idx,
                          const int32_t* offsets, void* x_perm, float* x_perm_scale,
                          int32_t* perm_token, int32_t* inv_pos, void* ws, size_t ws_bytes,
@@ -149,6 +151,26 @@ MOE_API moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm
                             const float* w_gu_scale, const void* w_down, const float* w_down_scale,
                             void* y, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The expert FFN with the dispatch copy fused into the gate/up GEMM: routed
+ * row r of expert e is read straight from x[perm_token[r]] while the GEMM
+ * stages its operand, so no x_perm is written or read (the single-GPU form of
+ * the dispatch step in "DeepSeek-V3 Overview and Key Innovations", Training
+ * Infrastructure and Optimization, folded into the experts of "DeepSeek-V3
+ * 技术报告要点" section 1).  Same arithmetic and bit-identical y as
+ * moe_expert_ffn on the rows that moe_permute would have written.
+ *   x           bf16 [T, d]           input (routed and shared experts)
+ *   perm_token  int32 [T*k]           from moe_permute (values in [0, T); an
+ *                                     out-of-range value sets MOE_ERR_DEVICE
+ *                                     and row 0 is read instead)
+ *   offsets, w_gate_up, w_gu_scale, w_down, w_down_scale, y: as moe_expert_ffn
+ * FP8: x is quantised per 1x128 tile to E4M3 inside the call (one copy of the
+ * T rows in `ws`), exactly as moe_permute quantises each permuted row. */
+MOE_API moe_status_t moe_expert_ffn_gather(const moe_shape_t* shape, const void* x, const int32_t* perm_token,
+                                           const int32_t* offsets, const void* w_gate_up,
+                                           const float* w_gu_scale, const void* w_down,
+                                           const float* w_down_scale, void* y, void* ws, size_t ws_bytes,
+                                           moe_stream_t stream);
+
 /* Combine: out[t] = sum_s y[T*k + s*T + t] + sum_j topk_gate[t, j] * y[inv_pos[t, j]]
  * (shared experts first, then slots j = 0..k-1, FP32 sum, bf16 store).
  *   y bf16 [T*k + S*T, d]; topk_gate f32 [T, k]; inv_pos int32 [T, k];
@@ -162,16 +184,26 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const 
 MOE_API moe_status_t moe_bias_update(const moe_shape_t* shape, const int32_t* counts, float* bias,
                              float gamma, moe_stream_t stream);
 
-/* The whole layer: moe_route, moe_permute, moe_expert_ffn, moe_combine and,
+/* The whole layer: moe_route, the dispatch, the expert FFN, moe_combine and,
  * when update_bias != 0, moe_bias_update with this batch's counts (after the
  * routing has used the old bias).  topk_idx, topk_gate and counts are optional
- * outputs (NULL keeps them in the workspace).  All intermediates live in `ws`. */
+ * outputs (NULL keeps them in the workspace).  All intermediates live in `ws`.
+ * The dispatch takes one of two forms (moe_forward_gathers tells which; both
+ * give bit-identical results): for batches with T*k <= 4096 moe_permute builds
+ * only the tables and moe_expert_ffn_gather reads the routed rows from x; for
+ * larger batches moe_permute writes the permuted copy and moe_expert_ffn reads
+ * it with whole-tile loads, which keeps the tensor cores fed better. */
 MOE_API moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_router,
                          float* bias, const float* logit_offset, const void* w_gate_up,
                          const float* w_gu_scale, const void* w_down, const float* w_down_scale,
                          void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts,
                          float gamma, int update_bias, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
+
+/* 1 if moe_forward fuses the dispatch into the expert GEMM for this shape
+ * (moe_permute tables only + moe_expert_ffn_gather), 0 if it writes the
+ * permuted copy (moe_permute + moe_expert_ffn), -1 for an invalid shape. */
+MOE_API int moe_forward_gathers(const moe_shape_t* shape);
 
 /* The expert FFN (same arguments and results as moe_expert_ffn) for callers
  * that cannot allocate device memory -- a plugin inside a host framework that

@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # every symbol include/moe.h declares
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
-           "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static"]
+           "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static",
+           "moe_expert_ffn_gather", "moe_forward_gathers"]
 
 
 class MoEError(RuntimeError):
@@ -47,11 +48,13 @@ _SIGS = {
     "moe_permute": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn_static": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_ffn_gather": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [ctypes.POINTER(Shape), _P, _P, _F, _P]),
     "moe_forward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P,
                          _SZ, _P]),
     "moe_quantize_weights_fp8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "moe_forward_gathers": (_I, [ctypes.POINTER(Shape)]),
     "moe_get_device_status": (_I, [_P, _P]),
     "moe_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -104,6 +107,14 @@ def make_shape(T, d, E, S, k, I, fp8=False, n_group=0, topk_group=0) -> Shape:
     return Shape(T, d, E, S, k, I, MOE_FP8_E4M3 if fp8 else MOE_BF16, n_group, topk_group)
 
 
+def forward_gathers(shape: Shape) -> bool:
+    """True if moe_forward reads routed rows straight from x for this shape."""
+    r = load().moe_forward_gathers(ctypes.byref(shape))
+    if r < 0:
+        raise MoEError("moe_forward_gathers", 1)
+    return r == 1
+
+
 def workspace_bytes(shape: Shape) -> int:
     return int(load().moe_workspace_bytes(ctypes.byref(shape)))
 
@@ -139,15 +150,28 @@ def moe_route(shape: Shape, x, w_router, bias, logit_offset=None, ws=None):
     return idx, gate, counts, offsets
 
 
-def moe_permute(shape: Shape, x, topk_idx, offsets, ws=None):
+def moe_permute(shape: Shape, x, topk_idx, offsets, ws=None, rows=True, x_perm=None, x_perm_scale=None):
+    """rows=False: only the permutation tables (x_perm and its scales are None).
+    x_perm / x_perm_scale: optional preallocated outputs."""
     T, d, E, k = shape.T, shape.d, shape.E, shape.k
+    fp8 = shape.dtype == MOE_FP8_E4M3
     _need(x, torch.bfloat16, (T, d), "x")
     _need(topk_idx, torch.int32, (T, k), "topk_idx")
     _need(offsets, torch.int32, (E + 1,), "offsets")
     ws = alloc_workspace(shape, x.device) if ws is None else ws
-    x_perm = torch.empty(T * k, d, dtype=_act_dtype(shape), device=x.device)
-    scale = (torch.empty(T * k, d // 128, dtype=torch.float32, device=x.device)
-             if shape.dtype == MOE_FP8_E4M3 else None)
+    if not rows:
+        x_perm = scale = None
+    else:
+        if x_perm is None:
+            x_perm = torch.empty(T * k, d, dtype=_act_dtype(shape), device=x.device)
+        _need(x_perm, _act_dtype(shape), (T * k, d), "x_perm")
+        scale = x_perm_scale
+        if fp8 and scale is None:
+            scale = torch.empty(T * k, d // 128, dtype=torch.float32, device=x.device)
+        if fp8:
+            _need(scale, torch.float32, (T * k, d // 128), "x_perm_scale")
+        else:
+            scale = None
     perm_token = torch.empty(T * k, dtype=torch.int32, device=x.device)
     inv_pos = torch.empty(T, k, dtype=torch.int32, device=x.device)
     _check("moe_permute", load().moe_permute(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(offsets),
@@ -157,7 +181,7 @@ def moe_permute(shape: Shape, x, topk_idx, offsets, ws=None):
 
 
 def moe_expert_ffn(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_down, w_gu_scale=None,
-                   w_down_scale=None, ws=None):
+                   w_down_scale=None, ws=None, y=None):
     T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
     wdt = _act_dtype(shape)
     _need(x_perm, wdt, (T * k, d), "x_perm")
@@ -170,10 +194,37 @@ def moe_expert_ffn(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_
         _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
         _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
     ws = alloc_workspace(shape, x.device) if ws is None else ws
-    y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    if y is None:
+        y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, torch.bfloat16, (T * k + S * T, d), "y")
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(shape), _ptr(x_perm), _ptr(x_perm_scale), _ptr(x), _ptr(offsets), _ptr(w_gate_up),
         _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def moe_expert_ffn_gather(shape: Shape, x, perm_token, offsets, w_gate_up, w_down, w_gu_scale=None,
+                          w_down_scale=None, ws=None, y=None):
+    """The expert FFN reading routed rows straight from x through perm_token."""
+    T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
+    wdt = _act_dtype(shape)
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(perm_token, torch.int32, (T * k,), "perm_token")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
+    _need(w_down, wdt, (E + S, d, I), "w_down")
+    if shape.dtype == MOE_FP8_E4M3:
+        _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
+        _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
+    ws = alloc_workspace(shape, x.device) if ws is None else ws
+    if y is None:
+        y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, torch.bfloat16, (T * k + S * T, d), "y")
+    _check("moe_expert_ffn_gather", load().moe_expert_ffn_gather(
+        ctypes.byref(shape), _ptr(x), _ptr(perm_token), _ptr(offsets), _ptr(w_gate_up), _ptr(w_gu_scale),
+        _ptr(w_down), _ptr(w_down_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
     return y
 
 

@@ -37,6 +37,14 @@ static bool shape_supported(const moe_shape_t& s) {
   return true;
 }
 
+// Which form of the dispatch moe_forward uses.  Reading the routed rows straight
+// from x inside the gate/up GEMM (TMA row gathers, 512 bytes per operation) saves
+// the permuted copy but keeps far fewer bytes in flight per SM than 32-row box
+// loads of a contiguous copy; measured on B300 it wins only while the batch is
+// small (T*k = 512: 0.030 ms against 0.053 ms; T*k = 2048: even; T*k = 24576:
+// 0.67 ms against 0.52 ms; T*k = 65536: 8.6 ms against 6.1 ms).
+bool forward_gathers(const moe_shape_t& s) { return (size_t)s.T * s.k <= kForwardGatherMaxRows; }
+
 WsLayout ws_layout(const moe_shape_t& s) {
   WsLayout L{};
   const size_t A = 1024;
@@ -53,8 +61,9 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.perm_token = o;  o = align_up(o + 4 * Tk, A);
   L.inv_pos = o;     o = align_up(o + 4 * Tk, A);
   L.sched = o;       o = align_up(o + Schedule::bytes(s.E + s.S), A);
-  L.x_perm = o;      o = align_up(o + Tk * s.d * es, A);
-  L.x_perm_scale = o; o = align_up(o + (f8 ? Tk * (s.d / 128) * 4 : 0), A);
+  const size_t xp_rows = forward_gathers(s) ? 0 : Tk;  // moe_forward's permuted copy of x
+  L.x_perm = o;      o = align_up(o + xp_rows * s.d * es, A);
+  L.x_perm_scale = o; o = align_up(o + (f8 ? xp_rows * (s.d / 128) * 4 : 0), A);
   L.xq = o;          o = align_up(o + (f8 ? (size_t)s.T * s.d : 0), A);
   L.xq_scale = o;    o = align_up(o + (f8 ? (size_t)s.T * (s.d / 128) * 4 : 0), A);
   L.h = o;           o = align_up(o + rows * s.I * es, A);
@@ -219,8 +228,9 @@ moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t*
   NvtxRange nvtx_range("moe_permute");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x || !topk_idx || !offsets || !x_perm || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
+  if (!x || !topk_idx || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (!x_perm && x_perm_scale) return MOE_ERR_INVALID_ARG;  // tables only: no rows, no scales
+  if (x_perm && s.dtype == MOE_FP8_E4M3 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
   return launch_permute(s, x, topk_idx, offsets, x_perm, x_perm_scale, perm_token, inv_pos, ws,
@@ -239,8 +249,23 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const 
   if (!aligned16(x_perm) || !aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
     return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
-  return launch_expert_ffn(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
+  return launch_expert_ffn(s, x_perm, x_perm_scale, x, nullptr, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
                            y, ws, (cudaStream_t)stream);
+}
+
+moe_status_t moe_expert_ffn_gather(const moe_shape_t* shape, const void* x, const int32_t* perm_token,
+                                   const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
+                                   const void* w_down, const float* w_down_scale, void* y, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_expert_ffn_gather");
+  MOE_TRY(validate_shape(shape));
+  const moe_shape_t& s = *shape;
+  if (!x || !perm_token || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_ws(s, ws, ws_bytes));
+  return launch_expert_ffn(s, nullptr, nullptr, x, perm_token, offsets, w_gate_up, w_gu_scale, w_down,
+                           w_down_scale, y, ws, (cudaStream_t)stream);
 }
 
 moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* topk_gate,
@@ -284,16 +309,30 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
   int32_t* off = reinterpret_cast<int32_t*>(w + L.offsets);
   int32_t* ptok = reinterpret_cast<int32_t*>(w + L.perm_token);
   int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv_pos);
-  void* xp = w + L.x_perm;
-  float* xps = s.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(w + L.x_perm_scale) : nullptr;
   void* y = w + L.y;
   cudaStream_t st = (cudaStream_t)stream;
   MOE_TRY(launch_route(s, x, w_router, bias, logit_offset, idx, gate, cnt, off, ws, st));
-  MOE_TRY(launch_permute(s, x, idx, off, xp, xps, ptok, inv, ws, st));
-  MOE_TRY(launch_expert_ffn(s, xp, xps, x, off, w_gate_up, w_gu_scale, w_down, w_down_scale, y, ws, st));
+  if (forward_gathers(s)) {
+    // dispatch fused into the gate/up GEMM: only the permutation tables are built,
+    // the GEMM gathers each routed row from x through perm_token
+    MOE_TRY(launch_permute(s, x, idx, off, nullptr, nullptr, ptok, inv, ws, st));
+    MOE_TRY(launch_expert_ffn(s, nullptr, nullptr, x, ptok, off, w_gate_up, w_gu_scale, w_down, w_down_scale, y,
+                              ws, st));
+  } else {
+    void* xp = w + L.x_perm;
+    float* xps = s.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(w + L.x_perm_scale) : nullptr;
+    MOE_TRY(launch_permute(s, x, idx, off, xp, xps, ptok, inv, ws, st));
+    MOE_TRY(launch_expert_ffn(s, xp, xps, x, nullptr, off, w_gate_up, w_gu_scale, w_down, w_down_scale, y, ws,
+                              st));
+  }
   MOE_TRY(launch_combine(s, y, gate, inv, out, st));
   if (update_bias) MOE_TRY(launch_bias_update(s, cnt, bias, gamma, st));
   return MOE_OK;
+}
+
+int moe_forward_gathers(const moe_shape_t* shape) {
+  if (!shape || !shape_valid(shape)) return -1;
+  return forward_gathers(*shape) ? 1 : 0;
 }
 
 moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q, float* w_scale,

@@ -89,6 +89,6 @@ extern "C" MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, 
   cudaStream_t cs = (cudaStream_t)stream;
   // the device status word must start clear; the rest is overwritten before use
   if (cudaMemsetAsync(scratch, 0, 256, cs) != cudaSuccess) return MOE_ERR_CUDA;
-  return moe::launch_expert_ffn(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
+  return moe::launch_expert_ffn(s, x_perm, x_perm_scale, x, nullptr, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
                                 y, scratch, cs);
 }

@@ -22,7 +22,13 @@
 //
 // Warp roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
 //   warp 0      TMA producer of this CTA's operand halves; all loads of a stage
-//               complete on the even CTA's barrier;
+//               complete on the even CTA's barrier.  In the gathering variant
+//               (the fused forward) the routed token rows are not read from a
+//               permuted copy but straight from x: each lane holds four of the
+//               chunk's token indices (from the permutation table) and issues
+//               one TMA row gather of those four rows per K block, landing in
+//               the same swizzled layout as a box load (the dispatch step of the
+//               pages' layer fused into the expert GEMM's operand load);
 //   warp 1      TMEM allocation; in the even CTA the single MMA-issuing thread,
 //               whose commits are multicast to both CTAs;
 //   warps 2-9   epilogue in two groups of four (one TMEM lane quadrant per
@@ -81,12 +87,16 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
   return ti.n > 0;
 }
 
-template <int MODE>
+// GATHER (gate/up only): routed token rows are gathered from x (map_xg: [x_rows, K]
+// bf16, box 64 x 1 row) through perm_token instead of read from map_b0.
+template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
-                       const __grid_constant__ CUtensorMap map_b1, const GroupInfo* __restrict__ groups,
-                       const int* __restrict__ tile_start, int G, int E, int K, int I, int d,
+                       const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_xg,
+                       const GroupInfo* __restrict__ groups, const int* __restrict__ tile_start, int G, int E, int K,
+                       int I, int d, const int32_t* __restrict__ perm_token, int x_rows,
                        uint16_t* __restrict__ out, int* __restrict__ status) {
+  static_assert(!GATHER || MODE == kGateUp, "row gather feeds the gate/up GEMM only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kStages * kStage);
@@ -123,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_b0);
     tma_prefetch_desc(&map_b1);
+    if (GATHER) tma_prefetch_desc(&map_xg);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
   tc_fence_before();
@@ -132,7 +143,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t full_leader = map_to_rank(smem_u32(full), 0);        // full[0] of the even CTA
   const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ---------------- producer with row gather (whole warp): lane 0 issues the weight
+    // loads (and the shared experts' contiguous token rows), lane q gathers this CTA's
+    // token rows 4q .. 4q + 3 of a routed chunk
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      TileInfo ti;
+      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+      const int nm = (ti.n + 15) & ~15;
+      const int half = nm / 2;  // token rows per CTA (multiple of 8)
+      const bool gat = !ti.shared_b;
+      const int nbox_mine = gat ? 0 : (half + kBoxRows - 1) / kBoxRows;
+      const uint32_t b_mine = gat ? half * 128u : nbox_mine * kBox;
+      const uint32_t bytes_pair = 2 * (2 * kATile + b_mine);  // both CTAs (same row count)
+      const int a0_row = ti.mp * 256 + rank * 128;  // gate rows of this CTA's 128 features
+      const int a1_row = I + a0_row;                // up rows of the same features
+      const int brow = ti.brow0 + rank * half;
+      const bool my_rows = gat && 4 * lane < half;
+      int tk[4] = {0, 0, 0, 0};
+      if (my_rows) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int row = rank * half + 4 * lane + u;  // padding rows repeat the chunk's first token
+          int t = __ldg(perm_token + ti.brow0 + (row < ti.n ? row : 0));
+          if (t < 0 || t >= x_rows) {
+            set_error(status, status + 1, MOE_ERR_DEVICE, kSiteGemmProducer);
+            t = 0;
+          }
+          tk[u] = t;
+        }
+      }
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages, r = it / kStages;
+        int waited = 1;
+        if (lane == 0)
+          waited = mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer) ? 1 : 0;
+        waited = __shfl_sync(0xffffffffu, waited, 0);
+        if (!waited) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * kStage;
+        const uint32_t fb = full_leader + s * 8;
+        const int kq = (kb + ti.mp * kKStagger) % nk;
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
+          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, ti.expert);
+          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, ti.expert);
+          for (int b = 0; b < nbox_mine; ++b)
+            tma_load_2d_pair(st + 2 * kATile + b * kBox, &map_b1, fb, kq * 64, brow + b * kBoxRows);
+          last_round[s] = r;
+        }
+        if (my_rows)
+          tma_gather4_pair(st + 2 * kATile + lane * 512, &map_xg, fb, kq * 64, tk[0], tk[1], tk[2], tk[3]);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer: this CTA's weight rows and half of the token rows
       uint32_t it = 0;
@@ -367,12 +435,14 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 
 
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
-                               const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
-                               const void* w_down, const float* w_down_scale, void* y, void* ws, cudaStream_t st) {
+                               const int32_t* perm_token, const int32_t* offsets, const void* w_gate_up,
+                               const float* w_gu_scale, const void* w_down, const float* w_down_scale, void* y,
+                               void* ws, cudaStream_t st) {
   if (s.T == 0) return MOE_OK;
   if (s.dtype == MOE_FP8_E4M3)
-    return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale, y,
-                                 ws, st);
+    return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, perm_token, offsets, w_gate_up, w_gu_scale, w_down,
+                                 w_down_scale, y, ws, st);
+  const bool gather = perm_token != nullptr;
   const WsLayout L = ws_layout(s);
   char* w = static_cast<char*>(ws);
   const int G = s.E + s.S;
@@ -390,25 +460,32 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
                                      status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
-  CUtensorMap m_wgu, m_xp, m_x, m_wd, m_h;
+  CUtensorMap m_wgu, m_xp, m_x, m_xg, m_wd, m_h;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map_3d(&m_wgu, w_gate_up, bf, 2, s.d, 2 * (uint64_t)s.I, G, 64, 128)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_xp, x_perm, bf, 2, s.d, Tk, 64, kBoxRows)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_x, x, bf, 2, s.d, s.T, 64, kBoxRows)) return MOE_ERR_CUDA;
+  if (gather) {  // routed rows gathered from x one row at a time; no permuted copy
+    if (!make_map_2d(&m_xg, x, bf, 2, s.d, s.T, 64, 1)) return MOE_ERR_CUDA;
+    m_xp = m_x;
+  } else {
+    if (!make_map_2d(&m_xp, x_perm, bf, 2, s.d, Tk, 64, kBoxRows)) return MOE_ERR_CUDA;
+    m_xg = m_x;
+  }
   if (!make_map_3d(&m_wd, w_down, bf, 2, s.I, s.d, G, 64, 128)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_h, h, bf, 2, s.I, rows, 64, kBoxRows)) return MOE_ERR_CUDA;
 
-  auto k_gu = expert_gemm_kernel<kGateUp>;
-  auto k_dn = expert_gemm_kernel<kDown>;
+  auto k_gu = gather ? expert_gemm_kernel<kGateUp, true> : expert_gemm_kernel<kGateUp, false>;
+  auto k_dn = expert_gemm_kernel<kDown, false>;
   if (cudaFuncSetAttribute(k_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaFuncSetAttribute(k_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   const int grid = pair_grid((const void*)k_gu, kThreads, kSmemBytes);
   if (grid <= 0) return MOE_ERR_CUDA;
-  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, groups, ts_gu, G, s.E, s.d, s.I, s.d, h, status);
+  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, m_xg, groups, ts_gu, G, s.E, s.d, s.I, s.d, perm_token,
+                                          s.T, h, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d,
+  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d, nullptr, 0,
                                           static_cast<uint16_t*>(y), status);
   return cuda_status(cudaGetLastError());
 }

@@ -15,6 +15,11 @@
 // Tile: M = 128 weight rows (two of them per tile, as in the bf16 kernel: gate
 // and up rows of the same 128 features, or two 128-channel blocks of W_down),
 // N <= 96 tokens of one group, K block = 128 bytes = one 128-byte swizzle row.
+// In the gathering variant (the fused forward) the routed token rows are read
+// straight from the E4M3 copy of x: lane q of the producer warp gathers rows
+// 4q .. 4q + 3 of the chunk with one TMA row gather per K block (token indices
+// from the permutation table), and the scales come from the per-token scale
+// rows -- the dispatch step fused into the operand load.
 // Warps: 0 TMA producer, 1 MMA issuer, 2-13 promotion/epilogue in three groups
 // of four (group g owns token columns [32g, 32g + 32), warp w TMEM lanes of
 // quadrant w % 4).  The gate/up epilogue computes h = silu(g) * u and
@@ -72,14 +77,19 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
   return ti.n > 0;
 }
 
-template <int MODE>
+// GATHER (gate/up only): routed rows are gathered from the E4M3 copy of x (map_xg:
+// [x_rows, K] bytes, box 128 x 1 row; scales sa1) through perm_token instead of
+// read from map_b0 / sa0.
+template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
-                           const __grid_constant__ CUtensorMap map_b1, const GroupInfo* __restrict__ groups,
-                           const int* __restrict__ tile_start, int G, int E, int K, int I, int d,
-                           const float* __restrict__ sa0, const float* __restrict__ sa1,
-                           const float* __restrict__ sw, int w_rows, uint8_t* __restrict__ out,
-                           float* __restrict__ out_scale, int* __restrict__ status) {
+                           const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_xg,
+                           const GroupInfo* __restrict__ groups, const int* __restrict__ tile_start, int G, int E,
+                           int K, int I, int d, const float* __restrict__ sa0, const float* __restrict__ sa1,
+                           const float* __restrict__ sw, int w_rows, const int32_t* __restrict__ perm_token,
+                           int x_rows, uint8_t* __restrict__ out, float* __restrict__ out_scale,
+                           int* __restrict__ status) {
+  static_assert(!GATHER || MODE == kGateUp, "row gather feeds the gate/up GEMM only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint16_t* stg = reinterpret_cast<uint16_t*>(smem + kStages * kStage);
@@ -118,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_b0);
     tma_prefetch_desc(&map_b1);
+    if (GATHER) tma_prefetch_desc(&map_xg);
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -125,7 +136,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ---------------- producer with row gather (whole warp): lane 0 issues the weight
+    // loads (and the shared experts' contiguous token rows), lane q gathers token rows
+    // 4q .. 4q + 3 of a routed chunk
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      TileInfo ti;
+      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+      const bool gat = !ti.shared_b;
+      const int nm = (ti.n + 15) & ~15;
+      const int nbox = gat ? 0 : (ti.n + kBoxRows - 1) / kBoxRows;
+      const uint32_t bytes = 2 * kATile + (gat ? nm * 128u : nbox * kBox);
+      const int a0 = ti.m * 128, a1 = I + ti.m * 128;
+      const bool my_rows = gat && 4 * lane < nm;
+      int tk[4] = {0, 0, 0, 0};
+      if (my_rows) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int row = 4 * lane + u;  // padding rows repeat the chunk's first token
+          int t = __ldg(perm_token + ti.brow0 + (row < ti.n ? row : 0));
+          if (t < 0 || t >= x_rows) {
+            set_error(status, status + 1, MOE_ERR_DEVICE, kSiteGemmProducer);
+            t = 0;
+          }
+          tk[u] = t;
+        }
+      }
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages, r = it / kStages;
+        int waited = 1;
+        if (lane == 0)
+          waited = mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer) ? 1 : 0;
+        waited = __shfl_sync(0xffffffffu, waited, 0);
+        if (!waited) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * kStage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_3d(st, &map_w, &full[s], kb * 128, a0, ti.expert);
+          tma_load_3d(st + kATile, &map_w, &full[s], kb * 128, a1, ti.expert);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(st + 2 * kATile + b * kBox, &map_b1, &full[s], kb * 128, ti.brow0 + b * kBoxRows);
+          last_round[s] = r;
+        }
+        if (my_rows) tma_gather4(st + 2 * kATile + lane * 512, &map_xg, &full[s], kb * 128, tk[0], tk[1], tk[2], tk[3]);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       uint32_t it = 0;
@@ -205,11 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has = c0 < ti.n;  // warp-uniform
       // scale factor computation for this thread (etid < 64): operand etid / 32, column etid % 32
       const int fop = etid >> 5, fcol = etid & 31;
-      const float* sa_src = ti.shared_b ? sa1 : sa0;
+      const float* sa_src = (GATHER || ti.shared_b) ? sa1 : sa0;
       const bool fvalid = etid < 64 && c0 + fcol < ti.n;
+      size_t sa_rowi = (size_t)(ti.brow0 + c0 + fcol);  // scale row: permuted row, or token
+      if (GATHER && !ti.shared_b && fvalid) {
+        const int t = __ldg(perm_token + ti.brow0 + c0 + fcol);
+        sa_rowi = (t < 0 || t >= x_rows) ? 0 : (size_t)t;
+      }
       const int wrow = MODE == kGateUp ? (fop == 0 ? ti.m : I / 128 + ti.m) : 2 * ti.m + fop;
       const float* sw_row = sw + ((size_t)ti.expert * wblk_rows + (wrow < wblk_rows ? wrow : 0)) * nk;
-      const float* sa_row = sa_src + (size_t)(ti.brow0 + c0 + fcol) * nk;
+      const float* sa_row = sa_src + sa_rowi * nk;
       float sa_next = fvalid ? __ldg(sa_row) : 0.0f;
       float sw_next = (etid < 64) ? __ldg(sw_row) : 0.0f;
       float acc_a[32], acc_b[32];
@@ -356,9 +422,10 @@ __global__ void __launch_bounds__(128) quant_rows_kernel(const uint4* __restrict
 }  // namespace
 
 moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
-                                   const void* x, const int32_t* offsets, const void* w_gate_up,
-                                   const float* w_gu_scale, const void* w_down, const float* w_down_scale, void* y,
-                                   void* ws, cudaStream_t st) {
+                                   const void* x, const int32_t* perm_token, const int32_t* offsets,
+                                   const void* w_gate_up, const float* w_gu_scale, const void* w_down,
+                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st) {
+  const bool gather = perm_token != nullptr;
   const WsLayout L = ws_layout(s);
   char* w = static_cast<char*>(ws);
   const int G = s.E + s.S;
@@ -376,32 +443,40 @@ moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, con
   schedule_kernel<<<1, 512, 0, st>>>(offsets, s.T, s.k, s.E, s.S, s.I / 128, (s.d + 255) / 256, kChunk, groups,
                                      ts_gu, ts_dn, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  if (s.S > 0) {
+  if (s.S > 0 || gather) {  // E4M3 copy of x: the shared experts' input, and the gather source
     quant_rows_kernel<<<s.T, 128, 0, st>>>(static_cast<const uint4*>(x), s.d, xq, xq_scale);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
 
-  CUtensorMap m_wgu, m_xp, m_x, m_wd, m_h;
+  CUtensorMap m_wgu, m_xp, m_x, m_xg, m_wd, m_h;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if (!make_map_3d(&m_wgu, w_gate_up, u8, 1, s.d, 2 * (uint64_t)s.I, G, 128, 128)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_xp, x_perm, u8, 1, s.d, Tk, 128, kBoxRows)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_x, xq, u8, 1, s.d, s.T, 128, kBoxRows)) return MOE_ERR_CUDA;
+  if (gather) {  // routed rows gathered from the E4M3 copy of x one row at a time
+    if (!make_map_2d(&m_xg, xq, u8, 1, s.d, s.T, 128, 1)) return MOE_ERR_CUDA;
+    m_xp = m_x;
+  } else {
+    if (!make_map_2d(&m_xp, x_perm, u8, 1, s.d, Tk, 128, kBoxRows)) return MOE_ERR_CUDA;
+    m_xg = m_x;
+  }
   if (!make_map_3d(&m_wd, w_down, u8, 1, s.I, s.d, G, 128, 128)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_h, hq, u8, 1, s.I, rows, 128, kBoxRows)) return MOE_ERR_CUDA;
 
   const int grid = sm_count();
   if (grid <= 0) return MOE_ERR_CUDA;
-  auto k_gu = expert_gemm_fp8_kernel<kGateUp>;
-  auto k_dn = expert_gemm_fp8_kernel<kDown>;
+  auto k_gu = gather ? expert_gemm_fp8_kernel<kGateUp, true> : expert_gemm_fp8_kernel<kGateUp, false>;
+  auto k_dn = expert_gemm_fp8_kernel<kDown, false>;
   if (cudaFuncSetAttribute(k_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaFuncSetAttribute(k_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, groups, ts_gu, G, s.E, s.d, s.I, s.d, x_perm_scale,
-                                           xq_scale, w_gu_scale, 2 * s.I, hq, h_scale, status);
+  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, m_xg, groups, ts_gu, G, s.E, s.d, s.I, s.d,
+                                           x_perm_scale, xq_scale, w_gu_scale, 2 * s.I, perm_token, s.T, hq, h_scale,
+                                           status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d, h_scale, h_scale,
-                                           w_down_scale, s.d, static_cast<uint8_t*>(y), nullptr, status);
+  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d, h_scale,
+                                           h_scale, w_down_scale, s.d, nullptr, 0, static_cast<uint8_t*>(y), nullptr,
+                                           status);
   return cuda_status(cudaGetLastError());
 }
 

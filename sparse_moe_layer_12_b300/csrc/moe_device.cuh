@@ -116,6 +116,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Row gather: four arbitrary rows r0..r3 (outer coordinate) of a 2D tensor map whose
+// box is one row high, columns [c0, c0 + box inner), written to shared memory one
+// after another (4 x box-inner bytes from dst).  With the 128-byte swizzle the
+// chunk order of each row follows its shared-memory address, so consecutive
+// gathers at 512-byte steps fill an operand tile exactly as one box load of the
+// same rows would.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
@@ -276,6 +291,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
       "%4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Row gather (as tma_gather4) into this CTA's shared memory, completing on a barrier
+// that may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int c0,
+                                                 int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 

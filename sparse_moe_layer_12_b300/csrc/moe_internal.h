@@ -18,6 +18,7 @@ constexpr int kMaxK = 16;
 constexpr int kRouterTileM = 128;  // tokens per router tile
 constexpr int kChunkMax = 256;     // tokens per expert-GEMM tile (tcgen05 N)
 constexpr int kBoxRows = 32;       // token rows per TMA box in the expert GEMM
+constexpr size_t kForwardGatherMaxRows = 4096;  // moe_forward gathers routed rows while T*k <= this
 
 // Failure-site ids recorded next to the status word (diagnostics only).
 enum Site : int {
@@ -57,6 +58,7 @@ struct WsLayout {
 };
 
 bool shape_valid(const moe_shape_t* s);
+bool forward_gathers(const moe_shape_t& s);  // moe_forward's dispatch form (see moe_forward_gathers)
 WsLayout ws_layout(const moe_shape_t& s);
 
 // status word helpers (the word lives at offset 0 of the workspace)
@@ -80,17 +82,20 @@ bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
 moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_router, const float* bias,
                           const float* logit_offset, int32_t* idx, float* gate, int32_t* counts,
                           int32_t* offsets, void* ws, cudaStream_t st);
+// x_perm == nullptr: only the permutation tables (perm_token, inv_pos), no row copies
 moe_status_t launch_permute(const moe_shape_t& s, const void* x, const int32_t* idx, const int32_t* offsets,
                             void* x_perm, float* x_perm_scale, int32_t* perm_token, int32_t* inv_pos, void* ws,
                             cudaStream_t st);
+// perm_token == nullptr: routed rows from x_perm (+ x_perm_scale); otherwise the
+// gate/up GEMM gathers them from x through perm_token and x_perm is unused
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
-                               const void* x, const int32_t* offsets, const void* w_gate_up,
-                               const float* w_gu_scale, const void* w_down, const float* w_down_scale,
-                               void* y, void* ws, cudaStream_t st);
+                               const void* x, const int32_t* perm_token, const int32_t* offsets,
+                               const void* w_gate_up, const float* w_gu_scale, const void* w_down,
+                               const float* w_down_scale, void* y, void* ws, cudaStream_t st);
 moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
-                                   const void* x, const int32_t* offsets, const void* w_gate_up,
-                                   const float* w_gu_scale, const void* w_down, const float* w_down_scale,
-                                   void* y, void* ws, cudaStream_t st);
+                                   const void* x, const int32_t* perm_token, const int32_t* offsets,
+                                   const void* w_gate_up, const float* w_gu_scale, const void* w_down,
+                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st);
 // per-group token counts, chunking (<= chunk_max tokens) and tile prefix sums (one block of 512 threads)
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
                                 int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,

@@ -138,6 +138,7 @@ moe_status_t launch_permute(const moe_shape_t& s, const void* x, const int32_t* 
   int* status = ws_status(ws);
   permute_rank_kernel<<<s.E, kRankThreads, 0, st>>>(idx, offsets, s.T, s.k, s.E, perm_token, inv_pos, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (x_perm == nullptr) return MOE_OK;  // tables only (the fused forward gathers rows in the GEMM)
   if (s.dtype == MOE_FP8_E4M3)
     permute_scatter_kernel<true><<<s.T, kScatterThreads, 0, st>>>(
         static_cast<const uint4*>(x), inv_pos, s.T, s.d, s.k, static_cast<uint8_t*>(x_perm), x_perm_scale, status);

@@ -36,8 +36,14 @@ def test_workspace_bytes(libmoe):
     n = B.workspace_bytes(s)
     # x_perm + h + y dominate: (T*k*d + rows*I + rows*d) * 2 bytes
     rows = 8192 * 8 + 8192
+    assert B.forward_gathers(s) is False
     assert n >= (8192 * 8 * 7168 + rows * 2048 + rows * 7168) * 2
     assert n < 1.01 * (8192 * 8 * 7168 + rows * 2048 + rows * 7168) * 2 + (1 << 24)
+    # decode-sized batches gather routed rows inside the GEMM: no permuted copy
+    small = B.make_shape(256, 7168, 256, 1, 8, 2048)
+    assert B.forward_gathers(small) is True
+    rows = 256 * 9
+    assert B.workspace_bytes(small) < 1.01 * (rows * 2048 + rows * 7168) * 2 + (1 << 24)
     assert B.workspace_bytes(B.make_shape(8192, 7000, 256, 1, 8, 2048)) == 0  # d % 128
     assert B.workspace_bytes(B.make_shape(16, 256, 4, 1, 5, 128)) == 0  # k > E
     f8 = B.workspace_bytes(B.make_shape(8192, 7168, 256, 1, 8, 2048, fp8=True))
@@ -70,3 +76,22 @@ def test_alignment_and_workspace_are_checked(libmoe):
     assert libmoe.moe_quantize_weights_fp8(1, 100, 128, p, p, p, None) == 1
     assert libmoe.moe_debug_wait_timeout(p, 0, None) == 1
     assert len(args) == 7
+
+
+def test_gather_entries_check_arguments(libmoe):
+    s = B.make_shape(256, 256, 16, 1, 2, 128)
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10002)
+    # moe_expert_ffn_gather: null perm_token, misaligned x, missing workspace
+    assert libmoe.moe_expert_ffn_gather(ctypes.byref(s), p, None, p, p, None, p, None, p, p, 1 << 30, None) == 1
+    assert libmoe.moe_expert_ffn_gather(ctypes.byref(s), odd, p, p, p, None, p, None, p, p, 1 << 30, None) == 3
+    assert libmoe.moe_expert_ffn_gather(ctypes.byref(s), p, p, p, p, None, p, None, p, None, 0, None) == 4
+    f8 = B.make_shape(256, 256, 16, 1, 2, 128, fp8=True)
+    assert libmoe.moe_expert_ffn_gather(ctypes.byref(f8), p, p, p, p, None, p, None, p, p, 1 << 30, None) == 1
+    # moe_permute tables only: scales without rows are rejected
+    assert libmoe.moe_permute(ctypes.byref(s), p, p, p, None, p, p, p, p, 1 << 30, None) == 1
+    # dispatch form: gathers for decode-sized batches, copy for large ones, -1 for bad shapes
+    assert libmoe.moe_forward_gathers(ctypes.byref(B.make_shape(512, 7168, 256, 1, 8, 2048))) == 1
+    assert libmoe.moe_forward_gathers(ctypes.byref(B.make_shape(8192, 7168, 256, 1, 8, 2048))) == 0
+    assert libmoe.moe_forward_gathers(ctypes.byref(B.make_shape(256, 200, 16, 1, 2, 128))) == -1
+    assert libmoe.moe_forward_gathers(None) == -1
