@@ -91,23 +91,51 @@ int sm_count() {
   return n;
 }
 
-int pair_grid(const void* kernel, int threads, size_t smem) {
-  const int sms = sm_count();
-  if (sms <= 0) return 0;
+int max_active_clusters(const void* kernel, int cluster, int threads, size_t smem) {
+  // the occupancy query costs host time on every call; cache it per device and launch shape
+  struct Entry {
+    int dev, cluster, threads, value;
+    const void* kernel;
+    size_t smem;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].dev == dev && cache[i].kernel == kernel && cache[i].cluster == cluster &&
+          cache[i].threads == threads && cache[i].smem == smem)
+        return cache[i].value;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
   attr.val.clusterDim.y = 1;
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters <= 0) return sms & ~1;
-  return 2 * clusters;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the failed query
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 64) cache[used++] = Entry{dev, cluster, threads, clusters, kernel, smem};
+  return clusters;
+}
+
+int pair_grid(const void* kernel, int threads, size_t smem) {
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  const int clusters = max_active_clusters(kernel, 2, threads, smem);
+  return clusters > 0 ? 2 * clusters : sms & ~1;
 }
 
 // ---------------------------------------------------------------- TMA descriptors

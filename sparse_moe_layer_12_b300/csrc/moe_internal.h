@@ -68,6 +68,8 @@ inline int* ws_status(void* ws) { return reinterpret_cast<int*>(ws); }
 moe_status_t check_ws(const moe_shape_t& s, void* ws, size_t ws_bytes);
 bool aligned16(const void* p);
 int sm_count();
+// clusters of `cluster` CTAs of `kernel` that fit on the GPU at once (0 if the query fails); cached
+int max_active_clusters(const void* kernel, int cluster, int threads, size_t smem);
 // grid (in CTAs) of a persistent kernel launched in clusters of 2: 2 x the clusters that fit at once
 int pair_grid(const void* kernel, int threads, size_t smem);
 moe_status_t cuda_status(cudaError_t e);
