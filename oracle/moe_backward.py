@@ -74,16 +74,38 @@ def backward(x, w_router, w_gate_up, w_down, idx, dout, S, logit_offset=None) ->
     Returns dx [T, d], dw_router [E, d], dw_gate_up [E+S, 2I, d], dw_down [E+S, d, I],
     and per (token, slot): s, gate, dgate, ds, dz [T, k].
     """
+    wgu = np.asarray(w_gate_up)
+    wd = np.asarray(w_down)
+    G = wgu.shape[0]
+    r = backward_lazy(x, w_router, lambda e: (wgu[e], wd[e]), idx, dout, G - S, S, logit_offset,
+                      dw_experts=range(G))
+    dw_gate_up = np.zeros(wgu.shape)
+    dw_down = np.zeros(wd.shape)
+    for e, (gu, dn) in r.pop("dw").items():
+        dw_gate_up[e] = gu
+        dw_down[e] = dn
+    return dict(r, dw_gate_up=dw_gate_up, dw_down=dw_down)
+
+
+def backward_lazy(x, w_router, get_expert, idx, dout, E, S, logit_offset=None, dw_experts=(),
+                  need_dx=True) -> dict:
+    """The same gradients with the expert weights fetched one expert at a time
+    (get_expert(e) -> (w_gate_up [2I, d], w_down [d, I])), for layers too large to
+    hold every expert in float64.
+
+    x, idx, dout may be any subset of the batch's tokens: dx, dz and the per-slot
+    values are per token, while the weight gradients returned in dw = {e: (dW_gate_up,
+    dW_down)} (experts in dw_experts) and dw_router sum over the given tokens only.
+    need_dx=False skips the experts outside dw_experts (dx, dgate, ds, dz and
+    dw_router are then not returned).
+    """
     x = _f64(x)
     dout = _f64(dout)
     wr = _f64(w_router)
     idx = np.asarray(idx)
     T, d = x.shape
-    E = wr.shape[0]
     k = idx.shape[1]
-    wgu = np.asarray(w_gate_up)
-    wd = np.asarray(w_down)
-    G = wgu.shape[0]
+    want = set(int(e) for e in dw_experts)
     z = (x[:, None, :] * wr[idx]).sum(axis=2)  # logits of the chosen experts only
     if logit_offset is not None:
         z = z + _f64(logit_offset)[idx]
@@ -91,32 +113,42 @@ def backward(x, w_router, w_gate_up, w_down, idx, dout, S, logit_offset=None) ->
     ssum = s.sum(axis=1, keepdims=True)
     gate = s / ssum
     dx = np.zeros((T, d))
-    dw_gate_up = np.zeros(wgu.shape)
-    dw_down = np.zeros(wd.shape)
     dgate = np.zeros((T, k))
+    dw = {}
     for sh in range(S):
-        g = swiglu_expert_backward(x, wgu[E + sh], wd[E + sh], dout)
+        if not need_dx and E + sh not in want:
+            continue
+        wgu_e, wd_e = get_expert(E + sh)
+        g = swiglu_expert_backward(x, wgu_e, wd_e, dout)
         dx += g["dx"]
-        dw_gate_up[E + sh] += g["dw_gate_up"]
-        dw_down[E + sh] += g["dw_down"]
+        if E + sh in want:
+            dw[E + sh] = (g["dw_gate_up"], g["dw_down"])
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
-        if tok.size == 0:
+        if tok.size == 0 or (not need_dx and e not in want):
             continue
+        wgu_e, wd_e = get_expert(e)
         xe = x[tok]
-        y = _forward_rows(xe, wgu[e], wd[e])
+        y = _forward_rows(xe, wgu_e, wd_e)
         dgate[tok, slot] = (dout[tok] * y).sum(axis=1)
-        g = swiglu_expert_backward(xe, wgu[e], wd[e], gate[tok, slot][:, None] * dout[tok])
+        g = swiglu_expert_backward(xe, wgu_e, wd_e, gate[tok, slot][:, None] * dout[tok])
         np.add.at(dx, tok, g["dx"])
-        dw_gate_up[e] += g["dw_gate_up"]
-        dw_down[e] += g["dw_down"]
+        if e in want:
+            dw[e] = (g["dw_gate_up"], g["dw_down"])
+    for e in want:  # experts without tokens here: zero gradients
+        if e not in dw:
+            wgu_e, wd_e = get_expert(e)
+            dw[e] = (np.zeros(np.shape(wgu_e)), np.zeros(np.shape(wd_e)))
+    out = dict(s=s, gate=gate, dw=dw)
+    if not need_dx:
+        return out
     ds = (dgate - (dgate * gate).sum(axis=1, keepdims=True)) / ssum
     dz = ds * s * (1.0 - s)
     dw_router = np.zeros(wr.shape)
     np.add.at(dw_router, idx.reshape(-1), (dz.reshape(-1, 1) * np.repeat(x, k, axis=0)))
     dx += (dz[:, :, None] * wr[idx]).sum(axis=1)
-    return dict(dx=dx, dw_router=dw_router, dw_gate_up=dw_gate_up, dw_down=dw_down, s=s, gate=gate,
-                dgate=dgate, ds=ds, dz=dz)
+    out.update(dx=dx, dw_router=dw_router, dgate=dgate, ds=ds, dz=dz)
+    return out
 
 
 def _forward_rows(x_rows, w_gate_up, w_down) -> np.ndarray:

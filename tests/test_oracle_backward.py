@@ -107,3 +107,21 @@ def test_single_dense_expert_against_autograd():
     np.testing.assert_allclose(g["dw_gate_up"][0], wgut.grad.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(g["dw_down"][0], wdt.grad.numpy(), rtol=1e-12, atol=1e-12)
     assert np.abs(g["dw_router"]).max() == 0.0
+
+
+def test_lazy_backward_on_token_subsets():
+    # the subset uses the GPU tests rely on: dx of sampled tokens, dW of one expert from its own tokens
+    x, wr, wgu, wd, idx, off = _tiny(T=12, E=5, S=1, k=2, seed=9)
+    dout = np.random.default_rng(3).standard_normal(x.shape)
+    full = BW.backward(x, wr, wgu, wd, idx, dout, 1, logit_offset=off)
+    get = lambda e: (wgu[e], wd[e])
+    tok = np.array([1, 4, 7])
+    sub = BW.backward_lazy(x[tok], wr, get, idx[tok], dout[tok], 5, 1, off)
+    np.testing.assert_allclose(sub["dx"], full["dx"][tok], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sub["dz"], full["dz"][tok], rtol=1e-13, atol=1e-13)
+    e = int(idx[0, 0])
+    mine = np.nonzero((idx == e).any(axis=1))[0]
+    one = BW.backward_lazy(x[mine], wr, get, idx[mine], dout[mine], 5, 1, off, dw_experts=[e], need_dx=False)
+    np.testing.assert_allclose(one["dw"][e][0], full["dw_gate_up"][e], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(one["dw"][e][1], full["dw_down"][e], rtol=1e-13, atol=1e-13)
+    assert "dx" not in one
