@@ -233,6 +233,40 @@ MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, const void*
 MOE_API moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q,
                                       float* w_scale, moe_stream_t stream);
 
+/* Backward pass of the layer for the routing the forward chose (the gradients
+ * that training needs; "DeepSeek-V3 详解" 2.2-2.3 for the layer, and
+ * "deepseek-v3-report", load-balancing paragraph: the selection bias only picks
+ * the experts and gets no gradient, so the chosen set is an input).  With
+ * a = x Wg^T, u = x Wu^T, h = silu(a) u, y = h Wd^T per expert and
+ * out[t] = sum_shared y + sum_j g_j y_j, g_j = s_j / sum_i s_i, s = sigmoid(z):
+ *   dx         bf16 [T, d]          out  d sum(out * dout) / dx
+ *   dw_router  f32  [E, d]          out  ... / d w_router
+ *   dw_gate_up bf16 [E+S, 2I, d]    out  ... / d w_gate_up (every expert, 0 if unused)
+ *   dw_down    bf16 [E+S, d, I]     out  ... / d w_down
+ * Inputs: x bf16 [T, d]; w_router bf16 [E, d]; logit_offset f32 [E] or NULL (as
+ * moe_route); w_gate_up bf16 [E+S, 2I, d]; its per-expert transpose
+ * w_gate_up_t bf16 [E+S, d, 2I] and w_down's w_down_t bf16 [E+S, I, d] (from
+ * moe_transpose_weights; w_down itself is not needed); topk_idx int32 [T, k]
+ * (moe_route's; distinct experts per token, values in [0, E)); dout bf16 [T, d]
+ * (the gradient of the layer output).  The affinities s of the chosen experts are
+ * recomputed in FP32; every GEMM accumulates in FP32 on the tensor cores; the
+ * intermediates a, u, h, dh and [da du] are rounded to bf16.  dtype must be
+ * MOE_BF16 (MOE_ERR_UNSUPPORTED otherwise).  Deterministic run to run.
+ * `ws` (moe_backward_workspace_bytes; 256-byte aligned, first 256 bytes zero
+ * before first use) holds every intermediate; bad topk_idx sets MOE_ERR_DEVICE. */
+MOE_API size_t moe_backward_workspace_bytes(const moe_shape_t* shape);
+MOE_API moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const void* w_router,
+                                  const float* logit_offset, const void* w_gate_up, const void* w_gate_up_t,
+                                  const void* w_down_t, const int32_t* topk_idx, const void* dout, void* dx,
+                                  float* dw_router, void* dw_gate_up, void* dw_down, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* w_t[g][c][r] = w[g][r][c] for bf16 w [G, R, C] (R % 64 == 0, C % 64 == 0):
+ * the transposed expert weights moe_backward reads.  Used once per weight
+ * update, like moe_quantize_weights_fp8. */
+MOE_API moe_status_t moe_transpose_weights(int G, int R, int C, const void* w, void* w_t,
+                                           moe_stream_t stream);
+
 /* Reads (synchronising `stream`) and clears the device status word in `ws`:
  * MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the read
  * itself fails).  `ws` must be a workspace used by the calls above. */

@@ -5,6 +5,12 @@
 //   gate/up:  h[r, f] = silu(X[r] . Wg[f]) * (X[r] . Wu[f])   (SiLU*mul fused)
 //   down:     y[r, c] = h[r] . Wd[c]
 //
+// The backward pass reuses the same tiles: "down" mode with transposed weights
+// gives the input gradients (dh = dy Wd, dx = [da du] [Wg; Wu]); "gate/up raw"
+// writes the two pre-activations instead of h; "weight gradient" mode computes
+// dW[g] = B_g^T A_g over a group's own K range (the group's tokens, transposed and
+// zero-padded to 64-token blocks by the caller), one output matrix per group.
+//
 // Every routed expert is a group of rows of x_perm; every shared expert is a
 // group over all T rows of x, scheduled in the same persistent launch.
 //
@@ -55,10 +61,19 @@ constexpr uint32_t kStgBytes = 2 * 32 * kStgStride * 2;  // one [32][136] tile p
 constexpr uint32_t kCtrl = 1024;
 constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 
-enum Mode : int { kGateUp = 0, kDown = 1 };
+// kGateUp     A = [Wg; Wu] of the group's expert, B = token rows (routed: in_row0,
+//             shared experts: map_b1), out = h (SwiGLU fused)
+// kDown       A = W_down, B = h rows at out_row0, out = y
+// kGateUpRaw  as kGateUp, out = [a | u] (width 2I) and out2 = h
+// kDgrad      A = a transposed weight, B = token rows as kGateUp (the shared experts'
+//             rows from map_b1), out = B A^T (width `d`)
+// kWgrad      A = one 2-D operand [M, K] (no expert index), B rows from in_row0, K
+//             range = the group's own 64-column blocks, out = B A^T per group
+enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4 };
 
 struct TileInfo {
   int g, mp, tok0, n, expert, brow0, out_row0;
+  int k0, nk;  // K blocks of the tile: [k0, k0 + nk) (nk < 0: all K / 64)
   bool shared_b;
 };
 
@@ -82,8 +97,11 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
   ti.n = min(gi.csize, gi.n - ti.tok0);
   ti.expert = gi.expert;
   ti.out_row0 = gi.out_row0 + ti.tok0;
-  ti.shared_b = (mode == kGateUp) && g >= E;
-  ti.brow0 = (mode == kGateUp ? gi.in_row0 : gi.out_row0) + ti.tok0;
+  ti.shared_b = (mode == kGateUp || mode == kGateUpRaw || mode == kDgrad) && g >= E;
+  ti.brow0 = (mode == kDown ? gi.out_row0 : gi.in_row0) + ti.tok0;
+  // K range in 64-element blocks: the whole K, or (weight gradient) the group's own
+  ti.k0 = mode == kWgrad ? gi.pad0 : 0;
+  ti.nk = mode == kWgrad ? gi.pad1 : -1;
   return ti.n > 0;
 }
 
@@ -95,7 +113,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_xg,
                        const GroupInfo* __restrict__ groups, const int* __restrict__ tile_start, int G, int E, int K,
                        int I, int d, const int32_t* __restrict__ perm_token, int x_rows,
-                       uint16_t* __restrict__ out, int* __restrict__ status) {
+                       uint16_t* __restrict__ out, uint16_t* __restrict__ out2, int* __restrict__ status) {
   static_assert(!GATHER || MODE == kGateUp, "row gather feeds the gate/up GEMM only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -115,7 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();  // 0 = the CTA that issues the MMAs
   const int pair = static_cast<int>(cluster_id_x());
   const int npairs = static_cast<int>(nclusters_x());
-  const int nk = K / 64;
+  const int nk_all = K / 64;
   const int total = __ldg(tile_start + G);
 
   if (threadIdx.x == 0) {
@@ -144,6 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
 
   if (warp == 0 && GATHER) {
+    const int nk = nk_all;
     // ---------------- producer with row gather (whole warp): lane 0 issues the weight
     // loads (and the shared experts' contiguous token rows), lane q gathers this CTA's
     // token rows 4q .. 4q + 3 of a routed chunk
@@ -208,12 +227,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < total && ok; tile += npairs) {
         TileInfo ti;
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+        const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         const int nm = (ti.n + 15) & ~15;
         const int half = nm / 2;  // token rows per CTA (multiple of 8)
         const int nbox_mine = (half + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes_pair = 2 * (2 * kATile + nbox_mine * kBox);  // both CTAs (same box count)
         int a0_row, a1_row;
-        if (MODE == kGateUp) {
+        if (MODE == kGateUp || MODE == kGateUpRaw) {
           a0_row = ti.mp * 256 + rank * 128;        // gate rows of this CTA's 128 features
           a1_row = I + ti.mp * 256 + rank * 128;    // up rows of the same features
         } else {
@@ -222,6 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const CUtensorMap* mb = ti.shared_b ? &map_b1 : &map_b0;
         const int brow = ti.brow0 + rank * half;
+        const int wexp = MODE == kWgrad ? 0 : ti.expert;  // weight gradient: A is one 2-D operand
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer)) {
@@ -230,10 +251,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + s * kStage;
           const uint32_t fb = full_leader + s * 8;
-          const int kq = (kb + ti.mp * kKStagger) % nk;
+          const int kq = ti.k0 + (kb + ti.mp * kKStagger) % nk;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
-          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, ti.expert);
-          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, ti.expert);
+          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, wexp);
+          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, wexp);
           for (int b = 0; b < nbox_mine; ++b)
             tma_load_2d_pair(st + 2 * kATile + b * kBox, mb, fb, kq * 64, brow + b * kBoxRows);
           last_round[s] = r;
@@ -250,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
         const int nm = (ti.n + 15) & ~15;
         const uint32_t idesc = idesc_bf16(256, nm);
+        const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         if (!mbar_wait(tmem_empty, (tl & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
         tc_fence_after();
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -312,9 +334,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_remote(tmem_empty_leader);
         }
         const int rows_here = min(32, ti.n - c0);
+        const bool zero = MODE == kWgrad && ti.nk == 0;  // a group without tokens: dW = 0
 #pragma unroll
-        for (int pass = 0; pass < (MODE == kGateUp ? 1 : 2); ++pass) {
-          if (MODE == kGateUp) {
+        for (int pass = 0; pass < (MODE == kGateUp ? 1 : MODE == kGateUpRaw ? 3 : 2); ++pass) {
+          if (MODE == kGateUp || (MODE == kGateUpRaw && pass == 2)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float g = __uint_as_float(ra[i]);
@@ -325,19 +348,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              sg[i * kStgStride + f] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(pass == 0 ? ra[i] : rb[i])));
+              sg[i * kStgStride + f] = __bfloat16_as_ushort(
+                  __float2bfloat16_rn(zero ? 0.0f : __uint_as_float(pass == 0 ? ra[i] : rb[i])));
           }
           named_bar_sync(1 + grp, 128);
           // 128 features x 2 bytes = 16 x 16-byte pieces per token row
           const int ch = etid & 15;
-          const int col = (MODE == kGateUp ? ti.mp * 256 + rank * 128 : ti.mp * 512 + pass * 256 + rank * 128) +
-                          ch * 8;
-          const int width = MODE == kGateUp ? I : d;
-          if (col < width) {
+          int col, width;
+          bool in_range;
+          uint16_t* dst = out;
+          if (MODE == kGateUp || MODE == kGateUpRaw) {
+            // raw: pass 0 a, pass 1 u (rows [a | u] of width 2I), pass 2 h into out2
+            const int feat = ti.mp * 256 + rank * 128 + ch * 8;
+            const bool raw_au = MODE == kGateUpRaw && pass < 2;
+            col = (raw_au ? pass * I : 0) + feat;
+            width = raw_au ? 2 * I : I;
+            if (MODE == kGateUpRaw && pass == 2) dst = out2;
+            in_range = feat < I;
+          } else {
+            col = ti.mp * 512 + pass * 256 + rank * 128 + ch * 8;
+            width = d;
+            in_range = col < d;
+          }
+          if (in_range) {
             for (int rr = etid >> 4; rr < rows_here; rr += 8) {
               const uint4 v = *reinterpret_cast<const uint4*>(sg + rr * kStgStride + ch * 8);
-              *reinterpret_cast<uint4*>(out + (size_t)(ti.out_row0 + c0 + rr) * width + col) = v;
+              *reinterpret_cast<uint4*>(dst + (size_t)(ti.out_row0 + c0 + rr) * width + col) = v;
             }
           }
           named_bar_sync(1 + grp, 128);
@@ -483,11 +519,36 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   const int grid = pair_grid((const void*)k_gu, kThreads, kSmemBytes);
   if (grid <= 0) return MOE_ERR_CUDA;
   k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, m_xg, groups, ts_gu, G, s.E, s.d, s.I, s.d, perm_token,
-                                          s.T, h, status);
+                                          s.T, h, nullptr, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d, nullptr, 0,
-                                          static_cast<uint16_t*>(y), status);
+                                          static_cast<uint16_t*>(y), nullptr, status);
   return cuda_status(cudaGetLastError());
+}
+
+moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
+                             const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
+                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st) {
+  const void* fn;
+  switch (mode) {
+    case GemmMode::kGateUpRaw: fn = (const void*)expert_gemm_kernel<kGateUpRaw, false>; break;
+    case GemmMode::kDgradShared: fn = (const void*)expert_gemm_kernel<kDgrad, false>; break;
+    case GemmMode::kDgradRows: fn = (const void*)expert_gemm_kernel<kDown, false>; break;
+    case GemmMode::kWgrad: fn = (const void*)expert_gemm_kernel<kWgrad, false>; break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int grid = pair_grid(fn, kThreads, kSmemBytes);
+  if (grid <= 0) return MOE_ERR_CUDA;
+  CUtensorMap mw = map_w, m0 = map_b0, m1 = map_b1, mg = map_b0;
+  const int32_t* no_perm = nullptr;
+  int x_rows = 0;
+  uint16_t* o = static_cast<uint16_t*>(out);
+  uint16_t* o2 = static_cast<uint16_t*>(out2);
+  void* args[] = {&mw, &m0, &m1, &mg, &groups, &tile_start, &G, &E, &K, &I, &width, &no_perm, &x_rows, &o, &o2,
+                  &status};
+  return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, kSmemBytes, st));
 }
 
 }  // namespace moe

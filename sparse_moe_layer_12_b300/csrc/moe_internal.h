@@ -31,6 +31,7 @@ enum Site : int {
   kSiteGemmTeardown = 14,
   kSitePermute = 21,
   kSiteSchedule = 22,
+  kSiteBackward = 31,
   kSiteDebug = 90,
 };
 
@@ -56,6 +57,18 @@ struct WsLayout {
   size_t x_perm, x_perm_scale, xq, xq_scale, h, h_scale, y;
   size_t total;
 };
+
+// Workspace of moe_backward (byte offsets; all 1024-aligned).  R = T*k routed rows,
+// RS = R + S*T rows with the shared experts'; kcap = columns of the transposed
+// operands (every expert's tokens padded to 64).
+struct BwdLayout {
+  size_t status, counts, offsets, perm_token, inv_pos, s, gate, gate_row, dgate_row, dz, dz_row;
+  size_t sched1, sched2, wsched_a, wsched_b, kb_start;
+  size_t x_perm, dout_perm, au, h, dh, dgu, dx_rows, xT, dyT, hT, dguT, rpart;
+  size_t total;
+};
+size_t bwd_kcap(const moe_shape_t& s);
+BwdLayout bwd_layout(const moe_shape_t& s);
 
 bool shape_valid(const moe_shape_t* s);
 bool forward_gathers(const moe_shape_t& s);  // moe_forward's dispatch form (see moe_forward_gathers)
@@ -102,6 +115,22 @@ moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, con
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
                                 int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,
                                 int* __restrict__ ts_dn, int* __restrict__ status);
+// Backward-pass launches of the grouped expert GEMM (one persistent launch each):
+//   kGateUpRaw    out = [a | u] rows (width 2I), out2 = h rows (width I); B routed
+//                 rows map_b0 at in_row0, shared experts' rows map_b1
+//   kDgradShared  out = B A^T (width `width`); B as kGateUpRaw, A = map_w [G][width][K]
+//   kDgradRows    out = B A^T (width `width`); B = map_b0 rows at out_row0
+//   kWgrad        out = B A^T per group over its K blocks [pad0, pad0 + pad1);
+//                 A = map_w [1][M][K], B = map_b0 rows at in_row0 + chunk
+enum class GemmMode : int { kGateUpRaw, kDgradShared, kDgradRows, kWgrad };
+moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
+                             const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
+                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st);
+moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_router, const float* logit_offset,
+                             const void* w_gate_up, const void* w_gate_up_t, const void* w_down_t,
+                             const int32_t* topk_idx, const void* dout, void* dx, float* dw_router, void* dw_gate_up,
+                             void* dw_down, void* ws, cudaStream_t st);
+moe_status_t launch_transpose_weights(int G, int R, int C, const void* w, void* w_t, cudaStream_t st);
 moe_status_t launch_combine(const moe_shape_t& s, const void* y, const float* gate, const int32_t* inv_pos,
                             void* out, cudaStream_t st);
 moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, float* bias, float gamma,

@@ -15,6 +15,7 @@ Distributions: x ~ N(0, 1); router weight ~ N(0, sigma_r); expert weights
 ~ N(0, 1/sqrt(fan_in)) (the second argument of N is a standard deviation);
 bias b = 0 or U(-0.05, 0.05); the skewed decode workload adds per-expert logit
 offsets o_i = A * r_i^(-1.1) for a seeded permutation r of 1..E (Zipf, s = 1.1).
+The backward pass takes an upstream gradient dout ~ N(0, 1) of the output's shape.
 """
 from __future__ import annotations
 
@@ -75,6 +76,7 @@ CONFIGS: dict[str, MoEConfig] = {
 
 # tensor ids mixed into the seeds
 _ID_X, _ID_WR, _ID_B, _ID_OFF, _ID_WGU, _ID_WD = 1, 2, 3, 4, 5, 6
+_ID_DOUT = 9
 
 
 def _gen(device, *parts: int) -> torch.Generator:
@@ -90,6 +92,13 @@ def make_x(cfg: MoEConfig, device="cpu", T: int | None = None) -> torch.Tensor:
     """x ~ N(0,1) as bf16 [T, d] (row-major)."""
     T = cfg.T if T is None else T
     g = _gen(device, cfg.seed, _ID_X, T)
+    return torch.randn(T, cfg.d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_dout(cfg: MoEConfig, device="cpu", T: int | None = None) -> torch.Tensor:
+    """Upstream gradient of the layer output, N(0,1) as bf16 [T, d]."""
+    T = cfg.T if T is None else T
+    g = _gen(device, cfg.seed, _ID_DOUT, T)
     return torch.randn(T, cfg.d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
