@@ -244,28 +244,22 @@ MOE_API moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w
  *   dw_gate_up bf16 [E+S, 2I, d]    out  ... / d w_gate_up (every expert, 0 if unused)
  *   dw_down    bf16 [E+S, d, I]     out  ... / d w_down
  * Inputs: x bf16 [T, d]; w_router bf16 [E, d]; logit_offset f32 [E] or NULL (as
- * moe_route); w_gate_up bf16 [E+S, 2I, d]; its per-expert transpose
- * w_gate_up_t bf16 [E+S, d, 2I] and w_down's w_down_t bf16 [E+S, I, d] (from
- * moe_transpose_weights; w_down itself is not needed); topk_idx int32 [T, k]
- * (moe_route's; distinct experts per token, values in [0, E)); dout bf16 [T, d]
- * (the gradient of the layer output).  The affinities s of the chosen experts are
- * recomputed in FP32; every GEMM accumulates in FP32 on the tensor cores; the
- * intermediates a, u, h, dh and [da du] are rounded to bf16.  dtype must be
- * MOE_BF16 (MOE_ERR_UNSUPPORTED otherwise).  Deterministic run to run.
- * `ws` (moe_backward_workspace_bytes; 256-byte aligned, first 256 bytes zero
- * before first use) holds every intermediate; bad topk_idx sets MOE_ERR_DEVICE. */
+ * moe_route); w_gate_up bf16 [E+S, 2I, d] and w_down bf16 [E+S, d, I] as the
+ * forward takes them (no transposed copies: the input-gradient GEMMs read them
+ * MN-major); topk_idx int32 [T, k] (moe_route's; distinct experts per token,
+ * values in [0, E)); dout bf16 [T, d] (the gradient of the layer output).
+ * The affinities of the chosen experts are recomputed in FP32; every GEMM
+ * accumulates in FP32 on the tensor cores; a, u, h, dy = g dout, dh, [da du]
+ * and each row's dx contribution are rounded to bf16.  dtype must be MOE_BF16
+ * (MOE_ERR_UNSUPPORTED otherwise).  Deterministic run to run.  `ws`
+ * (moe_backward_workspace_bytes; 256-byte aligned, first 256 bytes zero before
+ * first use) holds every intermediate; bad topk_idx sets MOE_ERR_DEVICE. */
 MOE_API size_t moe_backward_workspace_bytes(const moe_shape_t* shape);
 MOE_API moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const void* w_router,
-                                  const float* logit_offset, const void* w_gate_up, const void* w_gate_up_t,
-                                  const void* w_down_t, const int32_t* topk_idx, const void* dout, void* dx,
-                                  float* dw_router, void* dw_gate_up, void* dw_down, void* ws, size_t ws_bytes,
+                                  const float* logit_offset, const void* w_gate_up, const void* w_down,
+                                  const int32_t* topk_idx, const void* dout, void* dx, float* dw_router,
+                                  void* dw_gate_up, void* dw_down, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
-
-/* w_t[g][c][r] = w[g][r][c] for bf16 w [G, R, C] (R % 64 == 0, C % 64 == 0):
- * the transposed expert weights moe_backward reads.  Used once per weight
- * update, like moe_quantize_weights_fp8. */
-MOE_API moe_status_t moe_transpose_weights(int G, int R, int C, const void* w, void* w_t,
-                                           moe_stream_t stream);
 
 /* Reads (synchronising `stream`) and clears the device status word in `ws`:
  * MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the read

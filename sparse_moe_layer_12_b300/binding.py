@@ -23,8 +23,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
            "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static",
-           "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward",
-           "moe_transpose_weights"]
+           "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward"]
 
 
 class MoEError(RuntimeError):
@@ -57,8 +56,7 @@ _SIGS = {
     "moe_quantize_weights_fp8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
     "moe_forward_gathers": (_I, [ctypes.POINTER(Shape)]),
     "moe_backward_workspace_bytes": (_SZ, [ctypes.POINTER(Shape)]),
-    "moe_backward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_transpose_weights": (_I, [_I, _I, _I, _P, _P, _P]),
+    "moe_backward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_device_status": (_I, [_P, _P]),
     "moe_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -310,19 +308,6 @@ def moe_quantize_weights_fp8(w):
     return wq, sc
 
 
-def moe_transpose_weights(w, out=None):
-    """bf16 [G, R, C] -> its per-expert transpose [G, C, R] (the operand layout moe_backward reads)."""
-    if not (w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 3 and w.is_contiguous()):
-        raise ValueError("w must be a contiguous CUDA bf16 tensor [G, R, C]")
-    G, R, C = w.shape
-    if out is None:
-        out = torch.empty(G, C, R, dtype=torch.bfloat16, device=w.device)
-    else:
-        _need(out, torch.bfloat16, (G, C, R), "out")
-    _check("moe_transpose_weights", load().moe_transpose_weights(G, R, C, _ptr(w), _ptr(out), _stream()))
-    return out
-
-
 def backward_workspace_bytes(shape: Shape) -> int:
     return int(load().moe_backward_workspace_bytes(ctypes.byref(shape)))
 
@@ -336,16 +321,15 @@ def alloc_backward_workspace(shape: Shape, device="cuda") -> torch.Tensor:
     return ws
 
 
-def moe_backward(shape: Shape, x, w_router, w_gate_up, w_gate_up_t, w_down_t, topk_idx, dout, logit_offset=None,
-                 ws=None, out=None):
+def moe_backward(shape: Shape, x, w_router, w_gate_up, w_down, topk_idx, dout, logit_offset=None, ws=None,
+                 out=None):
     """Gradients of the layer for the routing topk_idx: (dx bf16 [T, d], dw_router f32 [E, d],
     dw_gate_up bf16 [E+S, 2I, d], dw_down bf16 [E+S, d, I]).  `out` may hold those four tensors."""
     T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
     _need(x, torch.bfloat16, (T, d), "x")
     _need(w_router, torch.bfloat16, (E, d), "w_router")
     _need(w_gate_up, torch.bfloat16, (E + S, 2 * I, d), "w_gate_up")
-    _need(w_gate_up_t, torch.bfloat16, (E + S, d, 2 * I), "w_gate_up_t")
-    _need(w_down_t, torch.bfloat16, (E + S, I, d), "w_down_t")
+    _need(w_down, torch.bfloat16, (E + S, d, I), "w_down")
     _need(topk_idx, torch.int32, (T, k), "topk_idx")
     _need(dout, torch.bfloat16, (T, d), "dout")
     if logit_offset is not None:
@@ -363,9 +347,8 @@ def moe_backward(shape: Shape, x, w_router, w_gate_up, w_gate_up_t, w_down_t, to
     _need(dwgu, torch.bfloat16, (E + S, 2 * I, d), "dw_gate_up")
     _need(dwd, torch.bfloat16, (E + S, d, I), "dw_down")
     _check("moe_backward", load().moe_backward(
-        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(w_gate_up), _ptr(w_gate_up_t),
-        _ptr(w_down_t), _ptr(topk_idx), _ptr(dout), _ptr(dx), _ptr(dwr), _ptr(dwgu), _ptr(dwd), _ptr(ws),
-        ws.numel(), _stream()))
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(w_gate_up), _ptr(w_down),
+        _ptr(topk_idx), _ptr(dout), _ptr(dx), _ptr(dwr), _ptr(dwgu), _ptr(dwd), _ptr(ws), ws.numel(), _stream()))
     return dx, dwr, dwgu, dwd
 
 

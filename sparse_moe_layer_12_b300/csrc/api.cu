@@ -384,40 +384,30 @@ static moe_status_t backward_supported(const moe_shape_t& s) {
   if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   const long long rows = (long long)s.T * s.k + (long long)s.S * s.T;
   if (rows * 2 * s.I >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
-  if (bwd_kcap(s) >= (size_t)(1u << 31)) return MOE_ERR_UNSUPPORTED;
+  if (bwd_kcap(s) >= (size_t)(1u << 31)) return MOE_ERR_UNSUPPORTED;  // row indices stay int
+  if ((long long)(s.E + s.S) * 2 * s.I >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
 moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const void* w_router, const float* logit_offset,
-                          const void* w_gate_up, const void* w_gate_up_t, const void* w_down_t,
-                          const int32_t* topk_idx, const void* dout, void* dx, float* dw_router, void* dw_gate_up,
-                          void* dw_down, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                          const void* w_gate_up, const void* w_down, const int32_t* topk_idx, const void* dout,
+                          void* dx, float* dw_router, void* dw_gate_up, void* dw_down, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
   NvtxRange nvtx_range("moe_backward");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   MOE_TRY(backward_supported(s));
-  if (!x || !w_router || !w_gate_up || !w_gate_up_t || !w_down_t || !topk_idx || !dout || !dx || !dw_router ||
-      !dw_gate_up || !dw_down)
+  if (!x || !w_router || !w_gate_up || !w_down || !topk_idx || !dout || !dx || !dw_router || !dw_gate_up ||
+      !dw_down)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_gate_up_t) ||
-      !aligned16(w_down_t) || !aligned16(dout) || !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw_gate_up) ||
-      !aligned16(dw_down))
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(dout) ||
+      !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw_gate_up) || !aligned16(dw_down))
     return MOE_ERR_ALIGNMENT;
   if (!ws) return MOE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGNMENT;
   if (ws_bytes < bwd_layout(s).total) return MOE_ERR_WORKSPACE;
-  return launch_backward(s, x, w_router, logit_offset, w_gate_up, w_gate_up_t, w_down_t, topk_idx, dout, dx,
-                         dw_router, dw_gate_up, dw_down, ws, (cudaStream_t)stream);
-}
-
-moe_status_t moe_transpose_weights(int G, int R, int C, const void* w, void* w_t, moe_stream_t stream) {
-  NvtxRange nvtx_range("moe_transpose_weights");
-  if (G < 0 || R < 0 || C < 0 || R % 64 || C % 64) return MOE_ERR_INVALID_ARG;
-  if ((long long)G * R * C >= (1ll << 40) || G > 65535 || R / 64 > 65535) return MOE_ERR_UNSUPPORTED;
-  if (G == 0 || R == 0 || C == 0) return MOE_OK;
-  if (!w || !w_t) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(w) || !aligned16(w_t)) return MOE_ERR_ALIGNMENT;
-  return launch_transpose_weights(G, R, C, w, w_t, (cudaStream_t)stream);
+  return launch_backward(s, x, w_router, logit_offset, w_gate_up, w_down, topk_idx, dout, dx, dw_router, dw_gate_up,
+                         dw_down, ws, (cudaStream_t)stream);
 }
 
 moe_status_t moe_get_device_status(void* ws, moe_stream_t stream) {

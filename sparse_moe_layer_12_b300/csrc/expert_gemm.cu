@@ -5,11 +5,13 @@
 //   gate/up:  h[r, f] = silu(X[r] . Wg[f]) * (X[r] . Wu[f])   (SiLU*mul fused)
 //   down:     y[r, c] = h[r] . Wd[c]
 //
-// The backward pass reuses the same tiles: "down" mode with transposed weights
-// gives the input gradients (dh = dy Wd, dx = [da du] [Wg; Wu]); "gate/up raw"
-// writes the two pre-activations instead of h; "weight gradient" mode computes
-// dW[g] = B_g^T A_g over a group's own K range (the group's tokens, transposed and
-// zero-padded to 64-token blocks by the caller), one output matrix per group.
+// The backward pass reuses the same tiles: "gate/up raw" writes the two
+// pre-activations next to h; "input gradient" mode reads the weight operand
+// MN-major (the stored W, contracted over its output dimension: dh = dy Wd,
+// dx = [da du] [Wg; Wu]), so no transposed weight copy exists; "weight gradient"
+// mode reads both operands MN-major from token-row buffers and computes
+// dW[g] = B_g^T A_g over the group's own rows (whole 64-row blocks, zero-padded
+// by the caller), one output matrix per group.
 //
 // Every routed expert is a group of rows of x_perm; every shared expert is a
 // group over all T rows of x, scheduled in the same persistent launch.
@@ -65,10 +67,11 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 //             shared experts: map_b1), out = h (SwiGLU fused)
 // kDown       A = W_down, B = h rows at out_row0, out = y
 // kGateUpRaw  as kGateUp, out = [a | u] (width 2I) and out2 = h
-// kDgrad      A = a transposed weight, B = token rows as kGateUp (the shared experts'
-//             rows from map_b1), out = B A^T (width `d`)
-// kWgrad      A = one 2-D operand [M, K] (no expert index), B rows from in_row0, K
-//             range = the group's own 64-column blocks, out = B A^T per group
+// kDgrad      A = W[g] stored [K][M] (map_w [G][K][M], read MN-major), B = token
+//             rows at in_row0 (K-major), out = B A (width `d`)
+// kWgrad      A = rows [K][M] of one buffer (map_w [1][rows][M], MN-major), B = rows
+//             [K][N] of another (map_b0 [rows][N], MN-major), K = the group's 64-row
+//             blocks [pad0, pad0 + pad1); out rows = N (chunks of 256), cols = M
 enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4 };
 
 struct TileInfo {
@@ -97,7 +100,7 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
   ti.n = min(gi.csize, gi.n - ti.tok0);
   ti.expert = gi.expert;
   ti.out_row0 = gi.out_row0 + ti.tok0;
-  ti.shared_b = (mode == kGateUp || mode == kGateUpRaw || mode == kDgrad) && g >= E;
+  ti.shared_b = (mode == kGateUp || mode == kGateUpRaw) && g >= E;
   ti.brow0 = (mode == kDown ? gi.out_row0 : gi.in_row0) + ti.tok0;
   // K range in 64-element blocks: the whole K, or (weight gradient) the group's own
   ti.k0 = mode == kWgrad ? gi.pad0 : 0;
@@ -230,8 +233,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         const int nm = (ti.n + 15) & ~15;
         const int half = nm / 2;  // token rows per CTA (multiple of 8)
-        const int nbox_mine = (half + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes_pair = 2 * (2 * kATile + nbox_mine * kBox);  // both CTAs (same box count)
+        // token operand: 32-row K-major boxes, or (weight gradient) 64-column MN-major boxes
+        const int nbox_mine = MODE == kWgrad ? half / 64 : (half + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes_pair = 2 * (2 * kATile + nbox_mine * (MODE == kWgrad ? 8192u : kBox));
         int a0_row, a1_row;
         if (MODE == kGateUp || MODE == kGateUpRaw) {
           a0_row = ti.mp * 256 + rank * 128;        // gate rows of this CTA's 128 features
@@ -242,7 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const CUtensorMap* mb = ti.shared_b ? &map_b1 : &map_b0;
         const int brow = ti.brow0 + rank * half;
-        const int wexp = MODE == kWgrad ? 0 : ti.expert;  // weight gradient: A is one 2-D operand
+        const int wexp = MODE == kWgrad ? 0 : ti.expert;  // weight gradient: A is one buffer
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer)) {
@@ -253,10 +257,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_leader + s * 8;
           const int kq = ti.k0 + (kb + ti.mp * kKStagger) % nk;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
-          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, wexp);
-          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, wexp);
-          for (int b = 0; b < nbox_mine; ++b)
-            tma_load_2d_pair(st + 2 * kATile + b * kBox, mb, fb, kq * 64, brow + b * kBoxRows);
+          if (MODE == kDgrad || MODE == kWgrad) {
+            // MN-major A: two 64-feature x 64-k boxes per 128 rows (k rows of 128 bytes)
+            tma_load_3d_pair(st, &map_w, fb, a0_row, kq * 64, wexp);
+            tma_load_3d_pair(st + 8192, &map_w, fb, a0_row + 64, kq * 64, wexp);
+            tma_load_3d_pair(st + kATile, &map_w, fb, a1_row, kq * 64, wexp);
+            tma_load_3d_pair(st + kATile + 8192, &map_w, fb, a1_row + 64, kq * 64, wexp);
+          } else {
+            tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, wexp);
+            tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, wexp);
+          }
+          if (MODE == kWgrad) {
+            for (int b = 0; b < nbox_mine; ++b)
+              tma_load_2d_pair(st + 2 * kATile + b * 8192, mb, fb, brow + b * 64, kq * 64);
+          } else {
+            for (int b = 0; b < nbox_mine; ++b)
+              tma_load_2d_pair(st + 2 * kATile + b * kBox, mb, fb, kq * 64, brow + b * kBoxRows);
+          }
           last_round[s] = r;
         }
       }
@@ -270,7 +287,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         TileInfo ti;
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
         const int nm = (ti.n + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(256, nm);
+        // MN-major operands: transpose bits 15 (A) and 16 (B) of the instruction descriptor
+        const uint32_t idesc = idesc_bf16(256, nm) | (MODE == kDgrad || MODE == kWgrad ? 1u << 15 : 0u) |
+                               (MODE == kWgrad ? 1u << 16 : 0u);
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         if (!mbar_wait(tmem_empty, (tl & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
         tc_fence_after();
@@ -286,10 +305,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b = a0 + 2 * kATile;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_k128(b + kk * 32);
+            // K-major: 16 k = 32 bytes along the row; MN-major: 16 k = 16 rows of 128 bytes
+            const uint64_t bd = MODE == kWgrad ? sdesc_mn128(b + kk * 2048) : sdesc_k128(b + kk * 32);
+            const bool amn = MODE == kDgrad || MODE == kWgrad;
+            const uint64_t ad0 = amn ? sdesc_mn128(a0 + kk * 2048) : sdesc_k128(a0 + kk * 32);
+            const uint64_t ad1 = amn ? sdesc_mn128(a1 + kk * 2048) : sdesc_k128(a1 + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
-            mma_bf16_pair(tmem, sdesc_k128(a0 + kk * 32), bd, idesc, acc);
-            mma_bf16_pair(tmem + 256, sdesc_k128(a1 + kk * 32), bd, idesc, acc);
+            mma_bf16_pair(tmem, ad0, bd, idesc, acc);
+            mma_bf16_pair(tmem + 256, ad1, bd, idesc, acc);
           }
           mma_commit_pair_mc(&empty[s], 0x3);  // stage s free in both CTAs
         }
@@ -532,8 +555,7 @@ moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUte
   const void* fn;
   switch (mode) {
     case GemmMode::kGateUpRaw: fn = (const void*)expert_gemm_kernel<kGateUpRaw, false>; break;
-    case GemmMode::kDgradShared: fn = (const void*)expert_gemm_kernel<kDgrad, false>; break;
-    case GemmMode::kDgradRows: fn = (const void*)expert_gemm_kernel<kDown, false>; break;
+    case GemmMode::kDgrad: fn = (const void*)expert_gemm_kernel<kDgrad, false>; break;
     case GemmMode::kWgrad: fn = (const void*)expert_gemm_kernel<kWgrad, false>; break;
     default: return MOE_ERR_INVALID_ARG;
   }

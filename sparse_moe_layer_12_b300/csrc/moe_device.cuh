@@ -166,6 +166,21 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle: each
+// 128-byte row holds 64 consecutive M (or N) elements of one k; 8 rows form a
+// 1 KB swizzle atom; consecutive groups of 8 k-rows are 1024 bytes apart (stride
+// byte offset) and consecutive 64-element blocks of M 8192 bytes apart (leading
+// byte offset: one 64 x 64 TMA box).
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor: dense, FP32 accumulator (bits 4-5 = 1), A/B format
 // (bits 7-9, 10-12), both operands K-major, N >> 3 at bits 17-22, M >> 4 at
 // bits 24-28.  kind::f16 format 1 = bf16; kind::f8f6f4 format 0 = E4M3.

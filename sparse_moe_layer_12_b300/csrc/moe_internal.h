@@ -58,13 +58,13 @@ struct WsLayout {
   size_t total;
 };
 
-// Workspace of moe_backward (byte offsets; all 1024-aligned).  R = T*k routed rows,
-// RS = R + S*T rows with the shared experts'; kcap = columns of the transposed
-// operands (every expert's tokens padded to 64).
+// Workspace of moe_backward (byte offsets; all 1024-aligned).  R = T*k routed rows;
+// kcap = rows of the row buffers (every expert's rows, routed and shared, padded to
+// a multiple of 64).
 struct BwdLayout {
-  size_t status, counts, offsets, perm_token, inv_pos, s, gate, gate_row, dgate_row, dz, dz_row;
-  size_t sched1, sched2, wsched_a, wsched_b, kb_start;
-  size_t x_perm, dout_perm, au, h, dh, dgu, dx_rows, xT, dyT, hT, dguT, rpart;
+  size_t status, counts, offsets, perm_token, inv_pos, s, gate, pinv, dz, gate_prow, dgate_prow, dz_prow;
+  size_t sched, wsched_a, wsched_b, kb_start;
+  size_t xp, dyp, au, h, dh, dgu, dx_rows;
   size_t total;
 };
 size_t bwd_kcap(const moe_shape_t& s);
@@ -115,22 +115,22 @@ moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, con
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
                                 int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,
                                 int* __restrict__ ts_dn, int* __restrict__ status);
-// Backward-pass launches of the grouped expert GEMM (one persistent launch each):
-//   kGateUpRaw    out = [a | u] rows (width 2I), out2 = h rows (width I); B routed
-//                 rows map_b0 at in_row0, shared experts' rows map_b1
-//   kDgradShared  out = B A^T (width `width`); B as kGateUpRaw, A = map_w [G][width][K]
-//   kDgradRows    out = B A^T (width `width`); B = map_b0 rows at out_row0
-//   kWgrad        out = B A^T per group over its K blocks [pad0, pad0 + pad1);
-//                 A = map_w [1][M][K], B = map_b0 rows at in_row0 + chunk
-enum class GemmMode : int { kGateUpRaw, kDgradShared, kDgradRows, kWgrad };
+// Backward-pass launches of the grouped expert GEMM (one persistent launch each);
+// every map has 128-byte swizzle:
+//   kGateUpRaw  out = [a | u] rows (width 2I), out2 = h rows (width I); A = map_w
+//               [G][2I][K] (box 64 x 128), B rows map_b0 / map_b1 at in_row0 (box 64 x 32)
+//   kDgrad      out = B W[g] (width `width`); map_w [G][K][width] (box 64 x 64, read
+//               MN-major), B = map_b0 rows at in_row0 (box 64 x 32)
+//   kWgrad      out[g] = B^T A over the group's rows [64 pad0, 64 (pad0 + pad1)):
+//               map_w [1][rows][M] and map_b0 [rows][N] (boxes 64 x 64, MN-major);
+//               out rows g * n + (N index), cols = M index (width `width`)
+enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad };
 moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
                              const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
                              int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st);
 moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_router, const float* logit_offset,
-                             const void* w_gate_up, const void* w_gate_up_t, const void* w_down_t,
-                             const int32_t* topk_idx, const void* dout, void* dx, float* dw_router, void* dw_gate_up,
-                             void* dw_down, void* ws, cudaStream_t st);
-moe_status_t launch_transpose_weights(int G, int R, int C, const void* w, void* w_t, cudaStream_t st);
+                             const void* w_gate_up, const void* w_down, const int32_t* topk_idx, const void* dout,
+                             void* dx, float* dw_router, void* dw_gate_up, void* dw_down, void* ws, cudaStream_t st);
 moe_status_t launch_combine(const moe_shape_t& s, const void* y, const float* gate, const int32_t* inv_pos,
                             void* out, cudaStream_t st);
 moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, float* bias, float gamma,

@@ -104,23 +104,18 @@ def test_backward_entries_check_arguments(libmoe):
     ws = ctypes.c_void_p(0x100000)
     big = 1 << 40
     n = libmoe.moe_backward_workspace_bytes(ctypes.byref(s))
-    # the transposed operands alone: x, dy (d rows), h (I rows), [da du] (2I rows) over >= T*k + S*T columns
-    assert n >= 2 * (256 * 2 + 256 + 16 * 63) * (2 * 256 + 3 * 128)
+    # the row buffers alone: x, dy, dx rows (d), [a u], [da du] (2I), h, dh (I) over >= T*k + S*T rows
+    assert n >= 2 * (256 * 2 + 256) * (3 * 256 + 6 * 128)
     assert libmoe.moe_backward_workspace_bytes(ctypes.byref(B.make_shape(256, 200, 16, 1, 2, 128))) == 0
-    args = [p, p, None] + [p] * 9  # x, w_router, logit_offset = NULL, w_gate_up ... dw_down
+    args = [p, p, None] + [p] * 8  # x, w_router, logit_offset = NULL, w_gate_up, w_down ... dw_down
     # null input, misaligned dout, small or missing workspace, FP8 layer
     bad = list(args)
-    bad[6] = None  # topk_idx
+    bad[5] = None  # topk_idx
     assert libmoe.moe_backward(ctypes.byref(s), *bad, ws, big, None) == 1
     bad = list(args)
-    bad[7] = odd  # dout
+    bad[6] = odd  # dout
     assert libmoe.moe_backward(ctypes.byref(s), *bad, ws, big, None) == 3
     assert libmoe.moe_backward(ctypes.byref(s), *args, ws, n - 1, None) == 4
     assert libmoe.moe_backward(ctypes.byref(s), *args, None, big, None) == 4
     f8 = B.make_shape(256, 256, 16, 1, 2, 128, fp8=True)
     assert libmoe.moe_backward(ctypes.byref(f8), *args, ws, big, None) == 2
-    # transpose: sizes must be multiples of 64, empty is a no-op, null rejected
-    assert libmoe.moe_transpose_weights(2, 100, 64, p, p, None) == 1
-    assert libmoe.moe_transpose_weights(0, 128, 64, None, None, None) == 0
-    assert libmoe.moe_transpose_weights(2, 128, 64, None, p, None) == 1
-    assert libmoe.moe_transpose_weights(2, 128, 64, odd, p, None) == 3

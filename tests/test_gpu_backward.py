@@ -63,18 +63,11 @@ def _inputs(cfg, dead=0):
 
 
 def _run(s, x, wr, off, wgu, wd, dout, idx, ws=None):
-    wgut = B.moe_transpose_weights(wgu)
-    wdt = B.moe_transpose_weights(wd)
     ws = B.alloc_backward_workspace(s) if ws is None else ws
-    g = B.moe_backward(s, x, wr, wgu, wgut, wdt, idx, dout, logit_offset=off, ws=ws)
+    g = B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
     torch.cuda.synchronize()
     assert B.moe_get_device_status(ws) == 0
     return g, ws
-
-
-def test_transpose_weights(libmoe):
-    w = torch.randn(3, 192, 320, device=DEV).to(torch.bfloat16)
-    assert torch.equal(B.moe_transpose_weights(w), w.transpose(1, 2).contiguous())
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -93,8 +86,7 @@ def test_backward_whole_tensors(libmoe, name):
     if dead:  # experts without tokens: exactly zero gradients
         assert not torch.any(dwgu[:dead]) and not torch.any(dwd[:dead]) and not torch.any(dwr[:dead])
     # deterministic: the same bits again
-    dx2, dwr2, dwgu2, dwd2 = B.moe_backward(s, x, wr, wgu, B.moe_transpose_weights(wgu),
-                                            B.moe_transpose_weights(wd), idx, dout, logit_offset=off, ws=ws)
+    dx2, dwr2, dwgu2, dwd2 = B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(dx, dx2) and torch.equal(dwr, dwr2) and torch.equal(dwgu, dwgu2) and torch.equal(dwd, dwd2)
 
