@@ -111,9 +111,9 @@ __global__ void __launch_bounds__(1024)
 // experts, then the shared ones) owns rows [64 kb_start[g], 64 kb_start[g+1]) of the
 // row buffers, its n tokens first.  groups: the token-row GEMMs (chunks of <= 256
 // tokens), with tile prefix sums for gate/up (I in 256-feature pairs), dh (I in
-// 512-blocks) and dx_rows (d in 512-blocks).  groups_a / groups_b: dW_down (d output
-// rows in chunks of 256, I in 512-blocks) and dW_gate_up (2I rows, d in 512-blocks),
-// K = the group's 64-row blocks.
+// 512-blocks) and dx_rows (d in 512-blocks).  groups_a / groups_b: dW_down (d rows in
+// chunks of 128, I columns in 512-blocks) and dW_gate_up (2I rows in chunks of 128, d
+// columns in 512-blocks), K = the group's 64-row blocks.
 __global__ void __launch_bounds__(512)
     bwd_schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int d, int I,
                         GroupInfo* __restrict__ groups, int* __restrict__ ts_gu, int* __restrict__ ts_dh,
@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(512)
   gi.csize = gi.nchunks ? (((ntok + gi.nchunks - 1) / gi.nchunks + 15) & ~15) : 16;
   gi.expert = g;
   ga.n = d;
-  ga.csize = kChunkMax;
-  ga.nchunks = (d + kChunkMax - 1) / kChunkMax;
+  ga.csize = 128;
+  ga.nchunks = d / 128;
   ga.out_row0 = g * d;
   gb.n = 2 * I;
-  gb.csize = kChunkMax;
-  gb.nchunks = (2 * I + kChunkMax - 1) / kChunkMax;
+  gb.csize = 128;
+  gb.nchunks = 2 * I / 128;
   gb.out_row0 = g * 2 * I;
   ga.expert = gb.expert = g;
   ga.pad0 = gb.pad0 = kb0;
@@ -537,6 +537,8 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
 
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap m_wgu, m_xp, m_wd_mn, m_dyp, m_wgu_mn, m_dgu, m_h_mn, m_dyp_mn, m_xp_mn, m_dgu_mn;
+  // weight gradients: A = the columns' operand of dW (h for dW_down, x for dW_gate_up) as
+  // [1][kcap][M] with 64 x 64 boxes, B = the rows' operand (dy, [da du]) as [kcap][N]
   const uint64_t I2 = 2 * (uint64_t)s.I;
   if (!make_map_3d(&m_wgu, w_gate_up, bf, 2, s.d, I2, G, 64, 128)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_xp, xp, bf, 2, s.d, kcap, 64, kBoxRows)) return MOE_ERR_CUDA;
@@ -570,10 +572,13 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
                                                                        groups, s.d, dw_router);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 7 weight gradients
+  CUtensorMap m_dwd, m_dwgu;  // outputs, stored from 32 x 128 staged tiles
+  if (!make_map_2d_plain(&m_dwd, dw_down, bf, 2, s.I, (uint64_t)G * s.d, 128, 32)) return MOE_ERR_CUDA;
+  if (!make_map_2d_plain(&m_dwgu, dw_gate_up, bf, 2, s.d, (uint64_t)G * I2, 128, 32)) return MOE_ERR_CUDA;
   MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_h_mn, m_dyp_mn, m_dyp_mn, ga, ts_a, G, s.E, (int)kcap, s.I, s.I, dw_down,
-                         nullptr, status, st));
+                         nullptr, status, st, &m_dwd));
   MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_xp_mn, m_dgu_mn, m_dgu_mn, gb, ts_b, G, s.E, (int)kcap, s.I, s.d,
-                         dw_gate_up, nullptr, status, st));
+                         dw_gate_up, nullptr, status, st, &m_dwgu));
   return MOE_OK;
 }
 

@@ -59,7 +59,9 @@ constexpr uint32_t kBTile = (kChunkMax / 2) * 128;  // this CTA's half of <= 256
 constexpr uint32_t kBox = kBoxRows * 128;      // one TMA box of token rows
 constexpr uint32_t kStage = 2 * kATile + kBTile;  // 48 KB
 constexpr int kStgStride = 136;                // staging row stride (bf16), 16-byte multiple
-constexpr uint32_t kStgBytes = 2 * 32 * kStgStride * 2;  // one [32][136] tile per epilogue group
+// epilogue staging: one [32][136] tile per group, or (weight gradient) two dense
+// [32][128] tiles per group, the sources of its TMA stores
+constexpr uint32_t kStgBytes = 2 * 2 * 32 * 128 * 2;
 constexpr uint32_t kCtrl = 1024;
 constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 
@@ -71,7 +73,13 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 //             rows at in_row0 (K-major), out = B A (width `d`)
 // kWgrad      A = rows [K][M] of one buffer (map_w [1][rows][M], MN-major), B = rows
 //             [K][N] of another (map_b0 [rows][N], MN-major), K = the group's 64-row
-//             blocks [pad0, pad0 + pad1); out rows = N (chunks of 256), cols = M
+//             blocks [pad0, pad0 + pad1); out[g] = B^T A: row = N index (chunks of
+//             128), col = M index (512 per tile, width `d`).  Short K (an expert's
+//             tokens) makes the epilogue as long as the MMAs, so a tile's two
+//             accumulators take 128 columns each and TMEM holds two tiles: the MMAs
+//             of the next tile run while this one drains; the output (the largest
+//             write of the backward) leaves through TMA stores (map_xg = the output
+//             map) of double-buffered staging tiles.
 enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4 };
 
 struct TileInfo {
@@ -80,19 +88,34 @@ struct TileInfo {
   bool shared_b;
 };
 
+// The group of a role's previous tile.  A role's tiles only grow and consecutive
+// ones mostly fall in the same group (hundreds of tiles per expert in the weight
+// gradients), so the lookup is skipped then.
+struct GroupCursor {
+  int g = -1, lo = 0, hi = 0;
+  GroupInfo gi;
+};
+
 // pair tile -> group, feature-block pair mp, token chunk
 __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups, const int* __restrict__ ts,
-                                            int G, int E, int tile, int mode, TileInfo& ti) {
-  int lo = 0, hi = G;  // find g with ts[g] <= tile < ts[g+1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(ts + mid) <= tile) lo = mid;
-    else hi = mid;
+                                            int G, int E, int tile, int mode, TileInfo& ti, GroupCursor& cur) {
+  if (cur.g < 0 || tile < cur.lo || tile >= cur.hi) {
+    // the largest g with ts[g] <= tile (ts[G] > tile); past the cached group if beyond it
+    int lo = cur.g >= 0 && tile >= cur.hi ? cur.g + 1 : 0, hi = G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(ts + mid) <= tile) lo = mid;
+      else hi = mid;
+    }
+    cur.g = lo;
+    cur.lo = __ldg(ts + lo);
+    cur.hi = __ldg(ts + lo + 1);
+    cur.gi = groups[lo];
   }
-  const int g = lo;
-  const GroupInfo gi = groups[g];
+  const int g = cur.g;
+  const GroupInfo& gi = cur.gi;
   if (gi.nchunks <= 0) return false;
-  const int local = tile - __ldg(ts + g);
+  const int local = tile - cur.lo;
   ti.g = g;
   ti.mp = local / gi.nchunks;
   const int c = local - ti.mp * gi.nchunks;
@@ -109,7 +132,8 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
 }
 
 // GATHER (gate/up only): routed token rows are gathered from x (map_xg: [x_rows, K]
-// bf16, box 64 x 1 row) through perm_token instead of read from map_b0.
+// bf16, box 64 x 1 row) through perm_token instead of read from map_b0.  kWgrad:
+// map_xg is the output map (no swizzle, box 128 x 32).
 template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
@@ -124,9 +148,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* ctrl = smem + kStages * kStage + kStgBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // [kStages], used in the even CTA
   uint64_t* empty = full + kStages;                    // [kStages], both CTAs
-  uint64_t* tmem_full = empty + kStages;               // both CTAs
-  uint64_t* tmem_empty = tmem_full + 1;                // even CTA: both CTAs' epilogues arrive
-  uint64_t* drain = tmem_empty + 1;
+  uint64_t* tmem_full = empty + kStages;               // [2] both CTAs
+  uint64_t* tmem_empty = tmem_full + 2;                // [2] even CTA: both CTAs' epilogues arrive
+  uint64_t* drain = tmem_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 132);
   volatile int* zero_flag = reinterpret_cast<volatile int*>(ctrl + 136);
@@ -145,8 +169,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
       last_round[s] = -1;
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 2 * 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 2 * 256);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     *zero_flag = 0;
@@ -162,7 +188,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t full_leader = map_to_rank(smem_u32(full), 0);        // full[0] of the even CTA
-  const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
+  const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);  // + 8 * buffer
+  // accumulator buffers: two of 256 columns (weight gradient), else one tile uses all 512
+  constexpr int kBufs = MODE == kWgrad ? 2 : 1;
 
   if (warp == 0 && GATHER) {
     const int nk = nk_all;
@@ -171,9 +199,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // token rows 4q .. 4q + 3 of a routed chunk
     uint32_t it = 0;
     bool ok = true;
+    GroupCursor cur;
     for (int tile = pair; tile < total && ok; tile += npairs) {
       TileInfo ti;
-      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
       const int nm = (ti.n + 15) & ~15;
       const int half = nm / 2;  // token rows per CTA (multiple of 8)
       const bool gat = !ti.shared_b;
@@ -227,9 +256,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------- TMA producer: this CTA's weight rows and half of the token rows
       uint32_t it = 0;
       bool ok = true;
+      GroupCursor cur;
       for (int tile = pair; tile < total && ok; tile += npairs) {
         TileInfo ti;
-        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         const int nm = (ti.n + 15) & ~15;
         const int half = nm / 2;  // token rows per CTA (multiple of 8)
@@ -283,16 +313,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------- MMA issuer (even CTA only)
       uint32_t it = 0, tl = 0;
       bool ok = true;
+      GroupCursor cur;
       for (int tile = pair; tile < total && ok; tile += npairs) {
         TileInfo ti;
-        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
+        if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
         const int nm = (ti.n + 15) & ~15;
         // MN-major operands: transpose bits 15 (A) and 16 (B) of the instruction descriptor
         const uint32_t idesc = idesc_bf16(256, nm) | (MODE == kDgrad || MODE == kWgrad ? 1u << 15 : 0u) |
                                (MODE == kWgrad ? 1u << 16 : 0u);
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
-        if (!mbar_wait(tmem_empty, (tl & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
+        const uint32_t buf = tl % kBufs, use = tl / kBufs;  // accumulator buffer, its earlier uses
+        if (!mbar_wait(&tmem_empty[buf], (use & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
         tc_fence_after();
+        const uint32_t acc0 = tmem + buf * 256;                             // feature block 0
+        const uint32_t acc1 = MODE == kWgrad ? acc0 + 128 : tmem + 256;      // feature block 1
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (!mbar_wait(&full[s], r & 1, abort_flag, status, status + 1, kSiteGemmMma)) {
@@ -311,13 +345,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t ad0 = amn ? sdesc_mn128(a0 + kk * 2048) : sdesc_k128(a0 + kk * 32);
             const uint64_t ad1 = amn ? sdesc_mn128(a1 + kk * 2048) : sdesc_k128(a1 + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
-            mma_bf16_pair(tmem, ad0, bd, idesc, acc);
-            mma_bf16_pair(tmem + 256, ad1, bd, idesc, acc);
+            mma_bf16_pair(acc0, ad0, bd, idesc, acc);
+            mma_bf16_pair(acc1, ad1, bd, idesc, acc);
           }
           mma_commit_pair_mc(&empty[s], 0x3);  // stage s free in both CTAs
         }
         if (!ok) break;
-        mma_commit_pair_mc(tmem_full, 0x3);
+        mma_commit_pair_mc(&tmem_full[buf], 0x3);
         ++tl;
       }
       mma_commit_pair(drain);
@@ -334,32 +368,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint16_t* sg = stg + grp * (32 * kStgStride);
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tl = 0;
+    uint32_t spass = 0;  // weight gradient: staged passes of this group (buffer = spass & 1)
+    GroupCursor cur;
     for (int tile = pair; tile < total; tile += npairs) {
       TileInfo ti;
-      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti)) continue;
-      if (!mbar_wait(tmem_full, tl & 1, abort_flag, status, status + 1, kSiteGemmEpi)) break;
+      if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
+      const uint32_t buf = tl % kBufs, use = tl / kBufs;
+      if (!mbar_wait(&tmem_full[buf], use & 1, abort_flag, status, status + 1, kSiteGemmEpi)) break;
       tc_fence_after();
+      const uint32_t empty_bar = tmem_empty_leader + 8 * buf;
       const int nm = (ti.n + 15) & ~15;
       const int nchunk = (nm + 31) / 32;
       const int mine = nchunk > grp ? (nchunk - grp + 1) / 2 : 0;
       if (mine == 0) {
         tc_fence_before();
-        mbar_arrive_remote(tmem_empty_leader);
+        mbar_arrive_remote(empty_bar);
       }
       for (int ci = 0; ci < mine; ++ci) {
         const int c0 = (grp + 2 * ci) * 32;
         uint32_t ra[32], rb[32];
-        tmem_ld32(tmem + lane_base + c0, ra);
-        tmem_ld32(tmem + lane_base + 256 + c0, rb);
+        tmem_ld32(tmem + lane_base + buf * 256 + c0, ra);
+        tmem_ld32(tmem + lane_base + (MODE == kWgrad ? buf * 256 + 128 : 256) + c0, rb);
         tmem_ld_wait();
         if (ci == mine - 1) {  // this group is done with TMEM for this tile
           tc_fence_before();
-          mbar_arrive_remote(tmem_empty_leader);
+          mbar_arrive_remote(empty_bar);
         }
         const int rows_here = min(32, ti.n - c0);
         const bool zero = MODE == kWgrad && ti.nk == 0;  // a group without tokens: dW = 0
 #pragma unroll
         for (int pass = 0; pass < (MODE == kGateUp ? 1 : MODE == kGateUpRaw ? 3 : 2); ++pass) {
+          if (MODE == kWgrad) {
+            uint16_t* sb = stg + (grp * 2 + (spass & 1)) * (32 * 128);
+            if (etid == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+            named_bar_sync(1 + grp, 128);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              sb[i * 128 + f] = __bfloat16_as_ushort(
+                  __float2bfloat16_rn(zero ? 0.0f : __uint_as_float(pass == 0 ? ra[i] : rb[i])));
+            fence_proxy_async_smem();
+            named_bar_sync(1 + grp, 128);
+            if (etid == 0) {
+              const int col = ti.mp * 512 + pass * 256 + rank * 128;
+              if (col < d) tma_store_2d(&map_xg, sb, col, ti.out_row0 + c0);
+              bulk_commit();  // one group per pass, empty when nothing was stored
+            }
+            ++spass;
+            continue;
+          }
           if (MODE == kGateUp || (MODE == kGateUpRaw && pass == 2)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -404,6 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ++tl;
     }
+    if (MODE == kWgrad && etid == 0) bulk_wait_all();  // staging is read and the output written
   }
   __syncthreads();
   if (warp == 0 && lane == 0 && *abort_flag) {
@@ -551,7 +608,9 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
 
 moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
                              const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
-                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st) {
+                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st,
+                             const CUtensorMap* map_out) {
+  if (mode == GemmMode::kWgrad && !map_out) return MOE_ERR_INVALID_ARG;
   const void* fn;
   switch (mode) {
     case GemmMode::kGateUpRaw: fn = (const void*)expert_gemm_kernel<kGateUpRaw, false>; break;
@@ -563,7 +622,7 @@ moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUte
     return MOE_ERR_CUDA;
   const int grid = pair_grid(fn, kThreads, kSmemBytes);
   if (grid <= 0) return MOE_ERR_CUDA;
-  CUtensorMap mw = map_w, m0 = map_b0, m1 = map_b1, mg = map_b0;
+  CUtensorMap mw = map_w, m0 = map_b0, m1 = map_b1, mg = map_out ? *map_out : map_b0;
   const int32_t* no_perm = nullptr;
   int x_rows = 0;
   uint16_t* o = static_cast<uint16_t*>(out);

@@ -140,6 +140,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory into another CTA's of the cluster; completes as tx bytes on
 // the barrier `bar_cluster` in the destination CTA.
+// TMA store of a row-major shared-memory tile (box of the map) to global at {c0, c1}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N committed bulk groups are still reading their shared-memory source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until every committed bulk group has completed (writes included)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
                                                   uint32_t bar_cluster) {
   asm volatile(

@@ -90,6 +90,9 @@ moe_status_t cuda_status(cudaError_t e);
 // TMA descriptors (128-byte swizzle, zero fill out of bounds)
 bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                  uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+// the same without swizzle (row-major boxes in shared memory; TMA stores of staged tiles)
+bool make_map_2d_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                       uint64_t outer, uint32_t box_inner, uint32_t box_outer);
 bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                  uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
 
@@ -123,11 +126,14 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 //               MN-major), B = map_b0 rows at in_row0 (box 64 x 32)
 //   kWgrad      out[g] = B^T A over the group's rows [64 pad0, 64 (pad0 + pad1)):
 //               map_w [1][rows][M] and map_b0 [rows][N] (boxes 64 x 64, MN-major);
-//               out rows g * n + (N index), cols = M index (width `width`)
+//               out row out_row0 + (N index, chunks of 128), col = M index (width
+//               `width`, 512 per tile), written by TMA stores through map_out
+//               ([rows of all groups][width], no swizzle, box 128 x 32)
 enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad };
 moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
                              const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
-                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st);
+                             int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st,
+                             const CUtensorMap* map_out = nullptr);
 moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_router, const float* logit_offset,
                              const void* w_gate_up, const void* w_down, const int32_t* topk_idx, const void* dout,
                              void* dx, float* dw_router, void* dw_gate_up, void* dw_down, void* ws, cudaStream_t st);
