@@ -11,6 +11,7 @@ step, far more than the 126 MB L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3|mid|v3fp8|skew|tiny]
     python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+    python bench.py --only backward ...    (the layer's backward pass, one JSON line)
 
 Prints one JSON line (rank 0).  Multi-GPU (torchrun, one rank per GPU): every
 rank runs its own T tokens (weak scaling) and the per-expert counts are summed
@@ -43,7 +44,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--set", default="", help="override workload fields, e.g. T=512,E=16 (profiling slices)")
-    p.add_argument("--only", default="", choices=["", "route"], help="time one stage alone (profiling)")
+    p.add_argument("--only", default="", choices=["", "route", "backward"],
+                   help="time one stage alone: the router, or the layer's backward pass")
     return p.parse_args()
 
 
@@ -290,6 +292,48 @@ def run_route_only(args):
     gb = (cfg.T * cfg.d * 2 + cfg.E * cfg.d * 2 + cfg.T * cfg.k * 8) / 1e9
     print(json.dumps({"stage": "route", "workload": cfg.name, "ms": ms, "GB/s": gb / (ms / 1e3),
                       "tflops": 2 * cfg.T * cfg.d * cfg.E / (ms / 1e3) / 1e12}), flush=True)
+
+
+def run_backward_only(args):
+    """moe_backward alone on the workload: gradients of the layer for the routing moe_route
+    chose, with a seeded N(0, 1) upstream gradient.  Algorithmic GEMM work per step:
+    16 T (k + S) d I FLOPs (gate/up recomputed 4, dh 2, dx 4, dW_down 2, dW_gate_up 4)."""
+    import torch
+
+    from sparse_moe_layer_12_b300 import binding as B
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    cfg = _config(args)
+    dev = torch.device("cuda", 0)
+    x, wr, b = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
+    off = I.make_logit_offset(cfg, dev)
+    wgu, wd = I.make_experts(cfg, dev)
+    dout = I.make_dout(cfg, dev)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, False, cfg.n_group, cfg.topk_group)
+    idx, _, _, _ = B.moe_route(s, x, wr, b, off)
+    ws = B.alloc_backward_workspace(s, dev)
+    out = B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
+    for _ in range(args.warmup):
+        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
+    torch.cuda.synchronize()
+    clocks = Clocks()
+    clocks.start()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
+    e.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    status = B.moe_get_device_status(ws)
+    ms = a.elapsed_time(e) / args.steps
+    flops = 16.0 * cfg.T * (cfg.k + cfg.S) * cfg.d * cfg.I
+    pk, src = _peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"stage": "backward", "workload": cfg.name, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3), "gemm_tflops": tf,
+                      "frac_of_bf16_peak": tf / pk["bf16_tflops_sustained"], "peak": f"{src} sustained bf16",
+                      "device_status": status, "clocks": ck}), flush=True)
 
 
 def run_ours(args):
@@ -551,6 +595,8 @@ def main():
         run_reference(args)
     elif args.only == "route":
         run_route_only(args)
+    elif args.only == "backward":
+        run_backward_only(args)
     else:
         run_ours(args)
 
