@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(1024)
 // row buffers, its n tokens first.  groups: the token-row GEMMs (chunks of <= 256
 // tokens), with tile prefix sums for gate/up (I in 256-feature pairs), dh (I in
 // 512-blocks) and dx_rows (d in 512-blocks).  groups_a / groups_b: dW_down (d rows in
-// chunks of 128, I columns in 512-blocks) and dW_gate_up (2I rows in chunks of 128, d
+// chunks of 256, I columns in 512-blocks) and dW_gate_up (2I rows in chunks of 256, d
 // columns in 512-blocks), K = the group's 64-row blocks.
 __global__ void __launch_bounds__(512)
     bwd_schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int d, int I,
@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(512)
   gi.csize = gi.nchunks ? (((ntok + gi.nchunks - 1) / gi.nchunks + 15) & ~15) : 16;
   gi.expert = g;
   ga.n = d;
-  ga.csize = 128;
-  ga.nchunks = d / 128;
+  ga.csize = kChunkMax;
+  ga.nchunks = (d + kChunkMax - 1) / kChunkMax;
   ga.out_row0 = g * d;
   gb.n = 2 * I;
-  gb.csize = 128;
-  gb.nchunks = 2 * I / 128;
+  gb.csize = kChunkMax;
+  gb.nchunks = (2 * I + kChunkMax - 1) / kChunkMax;
   gb.out_row0 = g * 2 * I;
   ga.expert = gb.expert = g;
   ga.pad0 = gb.pad0 = kb0;

@@ -74,12 +74,12 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 // kWgrad      A = rows [K][M] of one buffer (map_w [1][rows][M], MN-major), B = rows
 //             [K][N] of another (map_b0 [rows][N], MN-major), K = the group's 64-row
 //             blocks [pad0, pad0 + pad1); out[g] = B^T A: row = N index (chunks of
-//             128), col = M index (512 per tile, width `d`).  Short K (an expert's
-//             tokens) makes the epilogue as long as the MMAs, so a tile's two
-//             accumulators take 128 columns each and TMEM holds two tiles: the MMAs
-//             of the next tile run while this one drains; the output (the largest
-//             write of the backward) leaves through TMA stores (map_xg = the output
-//             map) of double-buffered staging tiles.
+//             256), col = M index (512 per tile, width `d`).  K is short (one
+//             expert's tokens), so the output (the largest write of the backward)
+//             leaves through TMA stores (map_xg = the output map) of double-buffered
+//             staging tiles, and the epilogue is no longer the long pole.  (A ring of
+//             two 512 x 128 accumulators in TMEM, which lets the next tile's MMAs run
+//             while one drains, measured slower: it reads every A block twice as often.)
 enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4 };
 
 struct TileInfo {
@@ -189,8 +189,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t full_leader = map_to_rank(smem_u32(full), 0);        // full[0] of the even CTA
   const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);  // + 8 * buffer
-  // accumulator buffers: two of 256 columns (weight gradient), else one tile uses all 512
-  constexpr int kBufs = MODE == kWgrad ? 2 : 1;
+  // accumulator buffers in TMEM: one tile uses all 512 columns (the barrier and column
+  // arithmetic allows a ring of two 256-column tiles)
+  constexpr int kBufs = 1;
 
   if (warp == 0 && GATHER) {
     const int nk = nk_all;
@@ -326,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tmem_empty[buf], (use & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmMma)) break;
         tc_fence_after();
         const uint32_t acc0 = tmem + buf * 256;                             // feature block 0
-        const uint32_t acc1 = MODE == kWgrad ? acc0 + 128 : tmem + 256;      // feature block 1
+        const uint32_t acc1 = acc0 + (kBufs == 1 ? 256 : 128);              // feature block 1
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (!mbar_wait(&full[s], r & 1, abort_flag, status, status + 1, kSiteGemmMma)) {
@@ -388,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int c0 = (grp + 2 * ci) * 32;
         uint32_t ra[32], rb[32];
         tmem_ld32(tmem + lane_base + buf * 256 + c0, ra);
-        tmem_ld32(tmem + lane_base + (MODE == kWgrad ? buf * 256 + 128 : 256) + c0, rb);
+        tmem_ld32(tmem + lane_base + buf * 256 + (kBufs == 1 ? 256 : 128) + c0, rb);
         tmem_ld_wait();
         if (ci == mine - 1) {  // this group is done with TMEM for this tile
           tc_fence_before();

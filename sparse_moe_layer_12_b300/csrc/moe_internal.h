@@ -126,7 +126,7 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 //               MN-major), B = map_b0 rows at in_row0 (box 64 x 32)
 //   kWgrad      out[g] = B^T A over the group's rows [64 pad0, 64 (pad0 + pad1)):
 //               map_w [1][rows][M] and map_b0 [rows][N] (boxes 64 x 64, MN-major);
-//               out row out_row0 + (N index, chunks of 128), col = M index (width
+//               out row out_row0 + (N index, chunks of 256), col = M index (width
 //               `width`, 512 per tile), written by TMA stores through map_out
 //               ([rows of all groups][width], no swizzle, box 128 x 32)
 enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad };
