@@ -249,8 +249,8 @@ MOE_API moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w
  * MN-major); topk_idx int32 [T, k] (moe_route's; distinct experts per token,
  * values in [0, E)); dout bf16 [T, d] (the gradient of the layer output).
  * The affinities of the chosen experts are recomputed in FP32; every GEMM
- * accumulates in FP32 on the tensor cores; a, u, h, dy = g dout, dh, [da du]
- * and each row's dx contribution are rounded to bf16.  dtype must be MOE_BF16
+ * accumulates in FP32 on the tensor cores; a, u and dh are kept in FP32; h,
+ * dy = g dout, [da du] and each row's dx contribution are rounded to bf16.  dtype must be MOE_BF16
  * (MOE_ERR_UNSUPPORTED otherwise).  Deterministic run to run.  `ws`
  * (moe_backward_workspace_bytes; 256-byte aligned, first 256 bytes zero before
  * first use) holds every intermediate; bad topk_idx sets MOE_ERR_DEVICE. */

@@ -19,10 +19,11 @@
 // Steps on the caller's stream:
 //   1 counts, offsets, the schedules and the permutation tables
 //   2 per token: x to the token's rows, s and g, then dy = g dout to the same rows
-//   3 grouped tcgen05 GEMMs: [a | u] and h (gate/up); dh (W_down read MN-major)
-//   4 per row: dg, [da du]
+//   3 grouped tcgen05 GEMMs: FP32 [a | u] and bf16 h (gate/up); FP32 dh (W_down read
+//     MN-major)
+//   4 per row: <dh, h>, [da du] (the SwiGLU derivative from FP32 a, u, dh)
 //   5 grouped tcgen05 GEMM: dx_rows (W_gate_up read MN-major)
-//   6 per token: dz, dx; per expert: dW_router
+//   6 per token: dg = <dh, h> / g, dz, dx; per expert: dW_router
 //   7 tcgen05 weight-gradient GEMMs, both operands read MN-major from the rows
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -32,7 +33,6 @@ namespace moe {
 namespace {
 
 constexpr int kTokThreads = 128;
-constexpr int kRowThreads = 256;
 
 size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kTokThreads)
                          const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ offsets,
                          const int* __restrict__ kb_start, int T, int d, int k, int E, int S,
                          uint4* __restrict__ xp, uint4* __restrict__ dyp, float* __restrict__ s_out,
-                         float* __restrict__ gate_out, float* __restrict__ gate_prow, int32_t* __restrict__ pinv,
+                         float* __restrict__ gate_out, int32_t* __restrict__ pinv,
                          int* __restrict__ status) {
   __shared__ int es[kMaxK], rs[kMaxK], shr[kMaxS];
   __shared__ float gs[kMaxK];
@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(kTokThreads)
       gs[j] = g;
       s_out[(size_t)t * k + j] = sv[j];
       gate_out[(size_t)t * k + j] = g;
-      if (rs[j] >= 0) gate_prow[rs[j]] = g;
     }
   }
   __syncthreads();
@@ -275,29 +274,34 @@ __global__ void __launch_bounds__(kTokThreads)
   }
 }
 
-// Zero rows n .. 64 ceil(n / 64) - 1 of every group in x and dy (grid: groups x 64)
+// Zero rows n .. 64 ceil(n / 64) - 1 of every group in x, dy, h and [da du] (the
+// operands of the weight-gradient GEMMs; grid: groups x 64)
 __global__ void __launch_bounds__(128)
-    zero_pad_rows_kernel(const GroupInfo* __restrict__ groups, int d, uint4* __restrict__ xp,
-                         uint4* __restrict__ dyp) {
+    zero_pad_rows_kernel(const GroupInfo* __restrict__ groups, int d, int I, uint4* __restrict__ xp,
+                         uint4* __restrict__ dyp, uint4* __restrict__ h, uint4* __restrict__ dgu) {
   const GroupInfo gi = groups[blockIdx.x];
   const int i = gi.n + blockIdx.y;
   if (i >= ((gi.n + 63) & ~63)) return;
   const size_t row = (size_t)gi.in_row0 + i;
-  const int nvec = d / 8;
-  for (int v = threadIdx.x; v < nvec; v += 128) {
-    xp[row * nvec + v] = make_uint4(0, 0, 0, 0);
-    dyp[row * nvec + v] = make_uint4(0, 0, 0, 0);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int v = threadIdx.x; v < d / 8; v += 128) {
+    xp[row * (d / 8) + v] = z;
+    dyp[row * (d / 8) + v] = z;
+  }
+  for (int v = threadIdx.x; v < I / 8; v += 128) {
+    h[row * (I / 8) + v] = z;
+    dgu[row * (I / 4) + v] = z;
+    dgu[row * (I / 4) + I / 8 + v] = z;
   }
 }
 
-// One block per row (64 kb_start[G] rows): dg = <dh, h> / g (routed rows),
-// da = dh u silu'(a), du = dh silu(a); a pad row gets zero h and [da du].
-__global__ void __launch_bounds__(kRowThreads)
-    swiglu_bwd_kernel(const uint4* __restrict__ au, uint4* __restrict__ h, const uint4* __restrict__ dh,
-                      const float* __restrict__ gate_prow, const GroupInfo* __restrict__ groups,
-                      const int* __restrict__ kb_start, int G, int E, int I, uint4* __restrict__ dgu,
-                      float* __restrict__ dgate_prow) {
-  __shared__ float red[kRowThreads / 32];
+// One block per row (64 kb_start[G] rows; pad rows are skipped, zero already):
+// <dh, h> (routed rows), da = dh u silu'(a), du = dh silu(a) from FP32 a, u, dh.
+__global__ void __launch_bounds__(256)
+    swiglu_bwd_kernel(const float4* __restrict__ au, const uint2* __restrict__ h, const float4* __restrict__ dh,
+                      const GroupInfo* __restrict__ groups, const int* __restrict__ kb_start, int G, int E, int I,
+                      uint2* __restrict__ dgu, float* __restrict__ dhh_row) {
+  __shared__ float red[8];
   const size_t r = blockIdx.x;
   const int tid = threadIdx.x;
   const int kb = static_cast<int>(r >> 6);
@@ -308,49 +312,41 @@ __global__ void __launch_bounds__(kRowThreads)
     if (kb_start[mid] <= kb) lo = mid;
     else hi = mid;
   }
-  const int nvec = I / 8;
-  if ((int)(r - (size_t)kb_start[lo] * 64) >= groups[lo].n) {  // pad row
-    for (int v = tid; v < nvec; v += kRowThreads) {
-      h[r * nvec + v] = make_uint4(0, 0, 0, 0);
-      dgu[r * 2 * nvec + v] = make_uint4(0, 0, 0, 0);
-      dgu[r * 2 * nvec + nvec + v] = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  const bool routed = lo < E;
+  if ((int)(r - (size_t)kb_start[lo] * 64) >= groups[lo].n) return;  // pad row
+  const int n4 = I / 4;
   float part = 0.0f;
-  for (int v = tid; v < nvec; v += kRowThreads) {
-    float a[8], u[8], hh[8], dr[8], da[8], du[8];
-    bf16x8_f32(au[r * 2 * nvec + v], a);
-    bf16x8_f32(au[r * 2 * nvec + nvec + v], u);
-    bf16x8_f32(h[r * nvec + v], hh);
-    bf16x8_f32(dh[r * nvec + v], dr);
+  for (int v = tid; v < n4; v += 256) {
+    const float4 a = au[r * 2 * n4 + v], u = au[r * 2 * n4 + n4 + v], g = dh[r * n4 + v];
+    const uint2 hv = h[r * n4 + v];
+    const float av[4] = {a.x, a.y, a.z, a.w}, uv[4] = {u.x, u.y, u.z, u.w}, gv[4] = {g.x, g.y, g.z, g.w};
+    const float hh[4] = {__uint_as_float(hv.x << 16), __uint_as_float(hv.x & 0xffff0000u),
+                         __uint_as_float(hv.y << 16), __uint_as_float(hv.y & 0xffff0000u)};
+    float da[4], du[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      part = fmaf(dr[i], hh[i], part);
-      const float sa = sigmoidf_(a[i]);
-      da[i] = dr[i] * u[i] * (sa * (1.0f + a[i] * (1.0f - sa)));
-      du[i] = dr[i] * (a[i] * sa);
+    for (int i = 0; i < 4; ++i) {
+      part = fmaf(gv[i], hh[i], part);
+      const float sa = sigmoidf_(av[i]);
+      da[i] = gv[i] * uv[i] * (sa * (1.0f + av[i] * (1.0f - sa)));
+      du[i] = gv[i] * (av[i] * sa);
     }
-    dgu[r * 2 * nvec + v] = f32_bf16x8(da);
-    dgu[r * 2 * nvec + nvec + v] = f32_bf16x8(du);
+    dgu[r * 2 * n4 + v] = make_uint2(pack_bf16x2(da[0], da[1]), pack_bf16x2(da[2], da[3]));
+    dgu[r * 2 * n4 + n4 + v] = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
   }
   part = warp_sum(part);
   if ((tid & 31) == 0) red[tid >> 5] = part;
   __syncthreads();
-  if (tid == 0 && routed) {
+  if (tid == 0 && lo < E) {
     float sum = 0.0f;
-    for (int w = 0; w < kRowThreads / 32; ++w) sum += red[w];
-    const float g = gate_prow[r];
-    dgate_prow[r] = g > 0.0f ? sum / g : 0.0f;  // g = 0: s = 0, so dz = 0 whatever dg is
+    for (int w = 0; w < 8; ++w) sum += red[w];
+    dhh_row[r] = sum;
   }
 }
 
-// One block per token: dz of its k slots, then
+// One block per token: dg_j = <dh, h> / g_j of its k rows, dz, then
 // dx[t] = sum_shared dx_rows + sum_j dx_rows[row j] + sum_j dz_j w_router[e_j].
 __global__ void __launch_bounds__(kTokThreads)
     bwd_token_kernel(const float* __restrict__ s_in, const float* __restrict__ gate,
-                     const float* __restrict__ dgate_prow, const int32_t* __restrict__ idx,
+                     const float* __restrict__ dhh_row, const int32_t* __restrict__ idx,
                      const int32_t* __restrict__ pinv, const int* __restrict__ kb_start,
                      const uint4* __restrict__ wr, const uint4* __restrict__ dx_rows, int d, int k, int E, int S,
                      float* __restrict__ dz_out, float* __restrict__ dz_prow, uint4* __restrict__ dx) {
@@ -369,7 +365,8 @@ __global__ void __launch_bounds__(kTokThreads)
       rs[j] = e < 0 ? -1 : r;
       sv[j] = s_in[(size_t)t * k + j];
       gv[j] = gate[(size_t)t * k + j];
-      dg[j] = rs[j] >= 0 ? dgate_prow[rs[j]] : 0.0f;
+      // dh = g dout Wd, so <dout, y> = <dh, h> / g; g = 0 means s = 0 and dz = 0 whatever dg is
+      dg[j] = rs[j] >= 0 && gv[j] > 0.0f ? dhh_row[rs[j]] / gv[j] : 0.0f;
       ssum += sv[j];
       gdg = fmaf(gv[j], dg[j], gdg);
     }
@@ -458,7 +455,6 @@ BwdLayout bwd_layout(const moe_shape_t& s) {
   take(L.gate, 4 * R);
   take(L.pinv, 4 * R);
   take(L.dz, 4 * R);
-  take(L.gate_prow, 4 * kcap);
   take(L.dgate_prow, 4 * kcap);
   take(L.dz_prow, 4 * kcap);
   take(L.sched, sched);
@@ -467,9 +463,9 @@ BwdLayout bwd_layout(const moe_shape_t& s) {
   take(L.kb_start, 4 * (G + 1));
   take(L.xp, kcap * d * 2);
   take(L.dyp, kcap * d * 2);
-  take(L.au, kcap * 2 * I * 2);
+  take(L.au, kcap * 2 * I * 4);
   take(L.h, kcap * I * 2);
-  take(L.dh, kcap * I * 2);
+  take(L.dh, kcap * I * 4);
   take(L.dgu, kcap * 2 * I * 2);
   take(L.dx_rows, kcap * d * 2);
   L.total = o;
@@ -500,8 +496,7 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
   float* gate = static_cast<float*>(at(L.gate));
   int32_t* pinv = static_cast<int32_t*>(at(L.pinv));
   float* dz = static_cast<float*>(at(L.dz));
-  float* gate_prow = static_cast<float*>(at(L.gate_prow));
-  float* dgate_prow = static_cast<float*>(at(L.dgate_prow));
+  float* dhh_row = static_cast<float*>(at(L.dgate_prow));
   float* dz_prow = static_cast<float*>(at(L.dz_prow));
   GroupInfo* groups = static_cast<GroupInfo*>(at(L.sched));
   int* ts_gu = reinterpret_cast<int*>(groups + G);
@@ -530,9 +525,11 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
   // 2 rows of x and dy, s and g
   bwd_token_fwd_kernel<<<s.T, kTokThreads, 0, st>>>(
       static_cast<const uint4*>(x), static_cast<const uint4*>(dout), wr4, logit_offset, topk_idx, inv_pos, offsets,
-      kb_start, s.T, s.d, s.k, s.E, s.S, static_cast<uint4*>(xp), static_cast<uint4*>(dyp), sv, gate, gate_prow, pinv,
+      kb_start, s.T, s.d, s.k, s.E, s.S, static_cast<uint4*>(xp), static_cast<uint4*>(dyp), sv, gate, pinv,
       status);
-  zero_pad_rows_kernel<<<dim3(G, 64), 128, 0, st>>>(groups, s.d, static_cast<uint4*>(xp), static_cast<uint4*>(dyp));
+  zero_pad_rows_kernel<<<dim3(G, 64), 128, 0, st>>>(groups, s.d, s.I, static_cast<uint4*>(xp),
+                                                    static_cast<uint4*>(dyp), static_cast<uint4*>(h),
+                                                    static_cast<uint4*>(dgu));
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -551,21 +548,21 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
   if (!make_map_3d(&m_xp_mn, xp, bf, 2, s.d, kcap, 1, 64, 64)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_dgu_mn, dgu, bf, 2, I2, kcap, 64, 64)) return MOE_ERR_CUDA;
 
-  // 3 [a | u], h; dh
+  // 3 [a | u] (FP32), h; dh (FP32)
   MOE_RC(launch_gemm_bwd(GemmMode::kGateUpRaw, m_wgu, m_xp, m_xp, groups, ts_gu, G, s.E, s.d, s.I, s.d, au, h, status,
                          st));
-  MOE_RC(launch_gemm_bwd(GemmMode::kDgrad, m_wd_mn, m_dyp, m_dyp, groups, ts_dh, G, s.E, s.d, s.I, s.I, dh, nullptr,
+  MOE_RC(launch_gemm_bwd(GemmMode::kDgrad32, m_wd_mn, m_dyp, m_dyp, groups, ts_dh, G, s.E, s.d, s.I, s.I, dh, nullptr,
                          status, st));
-  // 4 dg, [da du] (and zero h, [da du] on pad rows)
-  swiglu_bwd_kernel<<<static_cast<unsigned>(kcap), kRowThreads, 0, st>>>(
-      static_cast<const uint4*>(au), static_cast<uint4*>(h), static_cast<const uint4*>(dh), gate_prow, groups,
-      kb_start, G, s.E, s.I, static_cast<uint4*>(dgu), dgate_prow);
+  // 4 <dh, h>, [da du]
+  swiglu_bwd_kernel<<<static_cast<unsigned>(kcap), 256, 0, st>>>(
+      static_cast<const float4*>(au), static_cast<const uint2*>(h), static_cast<const float4*>(dh), groups, kb_start,
+      G, s.E, s.I, static_cast<uint2*>(dgu), dhh_row);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 5 dx_rows
   MOE_RC(launch_gemm_bwd(GemmMode::kDgrad, m_wgu_mn, m_dgu, m_dgu, groups, ts_dx, G, s.E, 2 * s.I, s.I, s.d, dx_rows,
                          nullptr, status, st));
-  // 6 dz, dx; dW_router
-  bwd_token_kernel<<<s.T, kTokThreads, 0, st>>>(sv, gate, dgate_prow, topk_idx, pinv, kb_start, wr4,
+  // 6 dg, dz, dx; dW_router
+  bwd_token_kernel<<<s.T, kTokThreads, 0, st>>>(sv, gate, dhh_row, topk_idx, pinv, kb_start, wr4,
                                                 static_cast<const uint4*>(dx_rows), s.d, s.k, s.E, s.S, dz, dz_prow,
                                                 static_cast<uint4*>(dx));
   router_grad_kernel<<<dim3(s.E, (s.d / 8 + 127) / 128), 128, 0, st>>>(static_cast<const uint4*>(xp), dz_prow,

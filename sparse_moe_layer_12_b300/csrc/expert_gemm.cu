@@ -68,7 +68,7 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 // kGateUp     A = [Wg; Wu] of the group's expert, B = token rows (routed: in_row0,
 //             shared experts: map_b1), out = h (SwiGLU fused)
 // kDown       A = W_down, B = h rows at out_row0, out = y
-// kGateUpRaw  as kGateUp, out = [a | u] (width 2I) and out2 = h
+// kGateUpRaw  as kGateUp, out = FP32 [a | u] (width 2I) and out2 = h (bf16)
 // kDgrad      A = W[g] stored [K][M] (map_w [G][K][M], read MN-major), B = token
 //             rows at in_row0 (K-major), out = B A (width `d`)
 // kWgrad      A = rows [K][M] of one buffer (map_w [1][rows][M], MN-major), B = rows
@@ -80,7 +80,8 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 //             staging tiles, and the epilogue is no longer the long pole.  (A ring of
 //             two 512 x 128 accumulators in TMEM, which lets the next tile's MMAs run
 //             while one drains, measured slower: it reads every A block twice as often.)
-enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4 };
+// kDgrad32    as kDgrad, out = FP32 (width `d`), stored straight from registers
+enum Mode : int { kGateUp = 0, kDown = 1, kGateUpRaw = 2, kWgrad = 3, kDgrad = 4, kDgrad32 = 5 };
 
 struct TileInfo {
   int g, mp, tok0, n, expert, brow0, out_row0;
@@ -288,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_leader + s * 8;
           const int kq = ti.k0 + (kb + ti.mp * kKStagger) % nk;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
-          if (MODE == kDgrad || MODE == kWgrad) {
+          if (MODE == kDgrad || MODE == kDgrad32 || MODE == kWgrad) {
             // MN-major A: two 64-feature x 64-k boxes per 128 rows (k rows of 128 bytes)
             tma_load_3d_pair(st, &map_w, fb, a0_row, kq * 64, wexp);
             tma_load_3d_pair(st + 8192, &map_w, fb, a0_row + 64, kq * 64, wexp);
@@ -320,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
         const int nm = (ti.n + 15) & ~15;
         // MN-major operands: transpose bits 15 (A) and 16 (B) of the instruction descriptor
-        const uint32_t idesc = idesc_bf16(256, nm) | (MODE == kDgrad || MODE == kWgrad ? 1u << 15 : 0u) |
+        const uint32_t idesc = idesc_bf16(256, nm) | (MODE == kDgrad || MODE == kDgrad32 || MODE == kWgrad ? 1u << 15 : 0u) |
                                (MODE == kWgrad ? 1u << 16 : 0u);
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         const uint32_t buf = tl % kBufs, use = tl / kBufs;  // accumulator buffer, its earlier uses
@@ -342,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             // K-major: 16 k = 32 bytes along the row; MN-major: 16 k = 16 rows of 128 bytes
             const uint64_t bd = MODE == kWgrad ? sdesc_mn128(b + kk * 2048) : sdesc_k128(b + kk * 32);
-            const bool amn = MODE == kDgrad || MODE == kWgrad;
+            const bool amn = MODE == kDgrad || MODE == kDgrad32 || MODE == kWgrad;
             const uint64_t ad0 = amn ? sdesc_mn128(a0 + kk * 2048) : sdesc_k128(a0 + kk * 32);
             const uint64_t ad1 = amn ? sdesc_mn128(a1 + kk * 2048) : sdesc_k128(a1 + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
@@ -399,6 +400,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool zero = MODE == kWgrad && ti.nk == 0;  // a group without tokens: dW = 0
 #pragma unroll
         for (int pass = 0; pass < (MODE == kGateUp ? 1 : MODE == kGateUpRaw ? 3 : 2); ++pass) {
+          if ((MODE == kGateUpRaw && pass < 2) || MODE == kDgrad32) {
+            // FP32 rows straight from registers (a warp writes 32 consecutive features,
+            // 128 bytes, of one row per store): a (pass 0) and u (pass 1) of the raw
+            // gate/up into [a | u] of width 2I, or the two 256-feature blocks of kDgrad32
+            const int F = MODE == kDgrad32 ? ti.mp * 512 + pass * 256 + rank * 128 + f
+                                           : ti.mp * 256 + rank * 128 + f;
+            const int lim = MODE == kDgrad32 ? d : I;
+            const int wo = MODE == kDgrad32 ? d : 2 * I;
+            if (F < lim) {
+              float* o = reinterpret_cast<float*>(out) + (size_t)(ti.out_row0 + c0) * wo +
+                         (MODE == kDgrad32 ? 0 : pass * I) + F;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < rows_here) o[(size_t)i * wo] = __uint_as_float(pass == 0 ? ra[i] : rb[i]);
+            }
+            continue;
+          }
           if (MODE == kWgrad) {
             uint16_t* sb = stg + (grp * 2 + (spass & 1)) * (32 * 128);
             if (etid == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
@@ -617,6 +635,7 @@ moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUte
     case GemmMode::kGateUpRaw: fn = (const void*)expert_gemm_kernel<kGateUpRaw, false>; break;
     case GemmMode::kDgrad: fn = (const void*)expert_gemm_kernel<kDgrad, false>; break;
     case GemmMode::kWgrad: fn = (const void*)expert_gemm_kernel<kWgrad, false>; break;
+    case GemmMode::kDgrad32: fn = (const void*)expert_gemm_kernel<kDgrad32, false>; break;
     default: return MOE_ERR_INVALID_ARG;
   }
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)

@@ -62,7 +62,7 @@ struct WsLayout {
 // kcap = rows of the row buffers (every expert's rows, routed and shared, padded to
 // a multiple of 64).
 struct BwdLayout {
-  size_t status, counts, offsets, perm_token, inv_pos, s, gate, pinv, dz, gate_prow, dgate_prow, dz_prow;
+  size_t status, counts, offsets, perm_token, inv_pos, s, gate, pinv, dz, dgate_prow, dz_prow;
   size_t sched, wsched_a, wsched_b, kb_start;
   size_t xp, dyp, au, h, dh, dgu, dx_rows;
   size_t total;
@@ -120,7 +120,7 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
                                 int* __restrict__ ts_dn, int* __restrict__ status);
 // Backward-pass launches of the grouped expert GEMM (one persistent launch each);
 // every map has 128-byte swizzle:
-//   kGateUpRaw  out = [a | u] rows (width 2I), out2 = h rows (width I); A = map_w
+//   kGateUpRaw  out = FP32 [a | u] rows (width 2I), out2 = bf16 h rows (width I); A = map_w
 //               [G][2I][K] (box 64 x 128), B rows map_b0 / map_b1 at in_row0 (box 64 x 32)
 //   kDgrad      out = B W[g] (width `width`); map_w [G][K][width] (box 64 x 64, read
 //               MN-major), B = map_b0 rows at in_row0 (box 64 x 32)
@@ -129,7 +129,8 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 //               out row out_row0 + (N index, chunks of 256), col = M index (width
 //               `width`, 512 per tile), written by TMA stores through map_out
 //               ([rows of all groups][width], no swizzle, box 128 x 32)
-enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad };
+//   kDgrad32    as kDgrad, out = FP32 rows
+enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad, kDgrad32 };
 moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
                              const CUtensorMap& map_b1, const GroupInfo* groups, const int* tile_start, int G, int E,
                              int K, int I, int width, void* out, void* out2, int* status, cudaStream_t st,

@@ -6,15 +6,15 @@ V3-shaped layer, and run-to-run determinism.
 
 Tolerances.  Two measures per output: out_err (the largest error beyond the bf16
 rounding of the output itself, over the RMS of the reference) and the relative
-Frobenius error.  The kernels store a, u, dh, h, dy, [da du] and the per-row dx
-contributions in bf16 (relative rounding 2^-9 each) and accumulate every
-contraction in FP32.  The same roundings replayed in float64 (a model of the
-kernels' arithmetic, not of their code) give out_err 0.019 / 0.023 (dx), 0.008 /
-0.013 (dw_router), 0.045 / 0.099 (dw_gate_up: dh, a, u and [da du] rounded before
-the contraction) and 0.024 / 0.047 (dw_down: h and dy) on the tiny / mid1k
-layers; the maximum grows with the number of elements.  The bounds leave about
-1.5x over the larger figure; every Frobenius error of that model is below 0.5 %,
-and a wrong index or a dropped term moves it to O(1).
+Frobenius error.  The kernels keep a, u and dh in FP32, store h, dy = g dout,
+[da du] and the per-row dx contributions in bf16 (relative rounding 2^-9 each)
+and accumulate every contraction in FP32.  The same roundings replayed in float64
+(a model of the kernels' arithmetic, not of their code) give out_err 0.011 /
+0.012 (dx), 0.006 / 0.007 (dw_router), 0.021 / 0.054 (dw_gate_up) and 0.024 /
+0.047 (dw_down) on the tiny / mid1k layers, Frobenius errors below 0.5 %; the
+maximum grows with the number of elements.  The bounds leave about 1.5x over the
+larger of those and of the measured values; a wrong index or a dropped term
+moves the Frobenius error to O(1).
 """
 import numpy as np
 import pytest
@@ -27,8 +27,8 @@ from moe_testutil import np64, oracle_route, out_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL = {"dx": 4e-2, "dw_router": 2.5e-2, "dw_gate_up": 1.5e-1, "dw_down": 8e-2}
-TOL_FRO = 1e-2
+TOL = {"dx": 2.5e-2, "dw_router": 2e-2, "dw_gate_up": 8e-2, "dw_down": 8e-2}
+TOL_FRO = 6e-3
 
 
 def fro_err(got, ref) -> float:
