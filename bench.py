@@ -43,6 +43,7 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     p.add_argument("--set", default="", help="override workload fields, e.g. T=512,E=16 (profiling slices)")
     p.add_argument("--only", default="", choices=["", "route", "backward"],
                    help="time one stage alone: the router, or the layer's backward pass")
@@ -294,13 +295,50 @@ def run_route_only(args):
                       "tflops": 2 * cfg.T * cfg.d * cfg.E / (ms / 1e3) / 1e12}), flush=True)
 
 
-def run_backward_only(args):
-    """moe_backward alone on the workload: gradients of the layer for the routing moe_route
-    chose, with a seeded N(0, 1) upstream gradient.  Algorithmic GEMM work per step:
-    16 T (k + S) d I FLOPs (gate/up recomputed 4, dh 2, dx 4, dW_down 2, dW_gate_up 4)."""
+def _time_backward(cfg, x, wr, b, off, wgu, wd, steps, warmup):
+    """moe_backward on the workload: gradients of the layer for the routing moe_route chose
+    (selection bias b), with a seeded N(0, 1) upstream gradient; CUDA events around `steps`
+    calls.  Algorithmic GEMM work per call: 16 T (k + S) d I FLOPs (gate/up recomputed 4,
+    dh 2, dx 4, dW_down 2, dW_gate_up 4)."""
     import torch
 
     from sparse_moe_layer_12_b300 import binding as B
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, False, cfg.n_group, cfg.topk_group)
+    dout = I.make_dout(cfg, x.device)
+    idx, _, _, _ = B.moe_route(s, x, wr, b, off)
+    ws = B.alloc_backward_workspace(s, x.device)
+    out = B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
+    for _ in range(warmup):
+        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
+    torch.cuda.synchronize()
+    clocks = Clocks()
+    clocks.start()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
+    e.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    status = B.moe_get_device_status(ws)
+    ms = a.elapsed_time(e) / steps
+    flops = 16.0 * cfg.T * (cfg.k + cfg.S) * cfg.d * cfg.I
+    pk, src = _peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    del out, ws, dout
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3), "gemm_tflops": tf,
+            "frac_of_bf16_peak": tf / pk["bf16_tflops_sustained"], "peak": f"{src} sustained bf16",
+            "steps": steps, "warmup": warmup, "device_status": status, "clocks": ck,
+            "gpu_launches_per_step": 13}
+
+
+def run_backward_only(args):
+    """moe_backward alone on the workload (one JSON line)."""
+    import torch
+
     from sparse_moe_layer_12_b300 import inputs as I
 
     cfg = _config(args)
@@ -308,32 +346,8 @@ def run_backward_only(args):
     x, wr, b = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
     off = I.make_logit_offset(cfg, dev)
     wgu, wd = I.make_experts(cfg, dev)
-    dout = I.make_dout(cfg, dev)
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, False, cfg.n_group, cfg.topk_group)
-    idx, _, _, _ = B.moe_route(s, x, wr, b, off)
-    ws = B.alloc_backward_workspace(s, dev)
-    out = B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
-    for _ in range(args.warmup):
-        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
-    torch.cuda.synchronize()
-    clocks = Clocks()
-    clocks.start()
-    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws, out=out)
-    e.record()
-    torch.cuda.synchronize()
-    ck = clocks.stop()
-    status = B.moe_get_device_status(ws)
-    ms = a.elapsed_time(e) / args.steps
-    flops = 16.0 * cfg.T * (cfg.k + cfg.S) * cfg.d * cfg.I
-    pk, src = _peaks()
-    tf = flops / (ms / 1e3) / 1e12
-    print(json.dumps({"stage": "backward", "workload": cfg.name, "steps": args.steps, "warmup": args.warmup,
-                      "ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3), "gemm_tflops": tf,
-                      "frac_of_bf16_peak": tf / pk["bf16_tflops_sustained"], "peak": f"{src} sustained bf16",
-                      "device_status": status, "clocks": ck}), flush=True)
+    r = _time_backward(cfg, x, wr, b, off, wgu, wd, args.steps, args.warmup)
+    print(json.dumps({"stage": "backward", "workload": cfg.name, **r}), flush=True)
 
 
 def run_ours(args):
@@ -577,6 +591,10 @@ def run_ours(args):
             cc = c.float()
             loads.append(round(float(cc.max() / cc.mean()), 3))
         line["load_max_over_mean_per_step"] = loads
+    if world == 1 and not fp8 and not args.no_backward:
+        # the layer's backward pass on the same weights (a row beyond the forward's hot path;
+        # not part of `value`)
+        line["backward"] = _time_backward(cfg, x, wr, bias, off, wgu, wd, args.steps, args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         del ws, wgu, wd
         torch.cuda.empty_cache()

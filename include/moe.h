@@ -27,6 +27,9 @@
  *   - Arguments are validated before anything is launched; a non-OK status
  *     means nothing was enqueued.  No C++ exception crosses the ABI.
  *   - Row-major tensors must start on a 16-byte boundary.
+ *   - With T = 0 every buffer sized by the tokens (or the routed rows) may be
+ *     NULL; the calls then only produce what does not depend on tokens (zero
+ *     counts and offsets, an unchanged bias, zero weight gradients).
  *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 bits;
  *     FP8 tensors hold OCP E4M3 ("e4m3fn") bytes.
  *   - Errors found on the device (a wait that timed out, an index out of

@@ -75,6 +75,9 @@ WsLayout ws_layout(const moe_shape_t& s) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// a buffer with one entry per token (or per routed row) may be NULL when there are no tokens
+static inline bool tok(const void* p, const moe_shape_t& s) { return p != nullptr || s.T == 0; }
+
 moe_status_t check_ws(const moe_shape_t& s, void* ws, size_t ws_bytes) {
   if (!ws) return MOE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGNMENT;
@@ -256,7 +259,8 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_ro
   NvtxRange nvtx_range("moe_route");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x || !w_router || !bias || !topk_idx || !topk_gate || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!tok(x, s) || !w_router || !bias || !tok(topk_idx, s) || !tok(topk_gate, s) || !counts || !offsets)
+    return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
   return launch_route(s, x, w_router, bias, logit_offset, topk_idx, topk_gate, counts, offsets, ws,
@@ -269,7 +273,8 @@ moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t*
   NvtxRange nvtx_range("moe_permute");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x || !topk_idx || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (!tok(x, s) || !tok(topk_idx, s) || !offsets || !tok(perm_token, s) || !tok(inv_pos, s))
+    return MOE_ERR_INVALID_ARG;
   if (!x_perm && x_perm_scale) return MOE_ERR_INVALID_ARG;  // tables only: no rows, no scales
   if (x_perm && s.dtype == MOE_FP8_E4M3 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
@@ -285,8 +290,8 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const 
   NvtxRange nvtx_range("moe_expert_ffn");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x_perm || !x || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && (!x_perm_scale || !w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (!tok(x_perm, s) || !tok(x, s) || !offsets || !w_gate_up || !w_down || !tok(y, s)) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3 && (!tok(x_perm_scale, s) || !w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
     return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
@@ -301,7 +306,7 @@ moe_status_t moe_expert_ffn_gather(const moe_shape_t* shape, const void* x, cons
   NvtxRange nvtx_range("moe_expert_ffn_gather");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x || !perm_token || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (!tok(x, s) || !tok(perm_token, s) || !offsets || !w_gate_up || !w_down || !tok(y, s)) return MOE_ERR_INVALID_ARG;
   if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
@@ -314,7 +319,7 @@ moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* t
   NvtxRange nvtx_range("moe_combine");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!y || !topk_gate || !inv_pos || !out) return MOE_ERR_INVALID_ARG;
+  if (!tok(y, s) || !tok(topk_gate, s) || !tok(inv_pos, s) || !tok(out, s)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
   return launch_combine(s, y, topk_gate, inv_pos, out, (cudaStream_t)stream);
 }
@@ -336,7 +341,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
   NvtxRange nvtx_range("moe_forward");
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
-  if (!x || !w_router || !bias || !w_gate_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+  if (!tok(x, s) || !w_router || !bias || !w_gate_up || !w_down || !tok(out, s)) return MOE_ERR_INVALID_ARG;
   if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (update_bias && (!(gamma >= 0.0f) || gamma > 1.0f)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
@@ -410,8 +415,8 @@ moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const void* w
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   MOE_TRY(backward_supported(s));
-  if (!x || !w_router || !w_gate_up || !w_down || !topk_idx || !dout || !dx || !dw_router || !dw_gate_up ||
-      !dw_down)
+  if (!tok(x, s) || !w_router || !w_gate_up || !w_down || !tok(topk_idx, s) || !tok(dout, s) || !tok(dx, s) ||
+      !dw_router || !dw_gate_up || !dw_down)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(dout) ||
       !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw_gate_up) || !aligned16(dw_down))

@@ -119,3 +119,19 @@ def test_backward_entries_check_arguments(libmoe):
     assert libmoe.moe_backward(ctypes.byref(s), *args, None, big, None) == 4
     f8 = B.make_shape(256, 256, 16, 1, 2, 128, fp8=True)
     assert libmoe.moe_backward(ctypes.byref(f8), *args, ws, big, None) == 2
+
+
+def test_empty_batch_accepts_null_token_buffers(libmoe):
+    # T = 0: the token-sized pointers may be NULL (validation passes them and stops at the
+    # missing workspace, before anything is launched); with T > 0 they are required
+    p = ctypes.c_void_p(0x10000)
+    e = B.make_shape(0, 256, 16, 1, 2, 128)
+    t = B.make_shape(4, 256, 16, 1, 2, 128)
+    assert libmoe.moe_route(ctypes.byref(e), None, p, p, None, None, None, p, p, None, 0, None) == 4
+    assert libmoe.moe_route(ctypes.byref(t), None, p, p, None, None, None, p, p, None, 0, None) == 1
+    assert libmoe.moe_forward(ctypes.byref(e), None, p, p, None, p, None, p, None, None, None, None, None,
+                              ctypes.c_float(0.001), 1, None, 0, None) == 4
+    assert libmoe.moe_backward(ctypes.byref(e), None, p, None, p, p, None, None, None, p, p, p, None, 0,
+                               None) == 4
+    assert libmoe.moe_backward(ctypes.byref(t), None, p, None, p, p, None, None, None, p, p, p, None, 0,
+                               None) == 1

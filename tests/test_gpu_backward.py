@@ -126,3 +126,32 @@ def test_backward_v3_sampled(libmoe):
     # experts without tokens (if any) have zero gradients
     for z in np.nonzero(counts == 0)[0][:4]:
         assert not torch.any(dwgu[z]) and not torch.any(dwr[z])
+
+
+def test_backward_degenerate_layers(libmoe):
+    # every expert chosen by every token (k = E), no shared expert; gates normalise over all E
+    cfg = I.MoEConfig("allk", 96, 256, 4, 0, 4, 128, 0.05, seed=11)
+    s, x, wr, off, wgu, wd, dout, idx = _inputs(cfg)
+    (dx, dwr, dwgu, dwd), _ = _run(s, x, wr, off, wgu, wd, dout, idx)
+    ref = BW.backward(np64(x), np64(wr), np64(wgu), np64(wd), idx.cpu().numpy(), np64(dout), 0)
+    for n, g in (("dx", dx), ("dw_router", dwr), ("dw_gate_up", dwgu), ("dw_down", dwd)):
+        assert out_err(g, ref[n]) < TOL[n] and fro_err(g, ref[n]) < TOL_FRO, n
+
+
+def test_backward_no_tokens(libmoe):
+    # T = 0: nothing to differentiate, every weight gradient is zero
+    s = B.make_shape(0, 256, 8, 1, 2, 128)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    cfg = I.MoEConfig("empty", 0, 256, 8, 1, 2, 128, 0.05)
+    wr = I.make_router(cfg, DEV)
+    wgu, wd = I.make_experts(cfg, DEV)
+    idx = torch.empty(0, 2, dtype=torch.int32, device=DEV)
+    out = (torch.empty(0, 256, dtype=torch.bfloat16, device=DEV),
+           torch.full((8, 256), 7.0, device=DEV),
+           torch.full((9, 256, 256), 7.0, device=DEV).to(torch.bfloat16),
+           torch.full((9, 256, 128), 7.0, device=DEV).to(torch.bfloat16))
+    ws = B.alloc_backward_workspace(s)
+    dx, dwr, dwgu, dwd = B.moe_backward(s, x, wr, wgu, wd, idx, x, ws=ws, out=out)
+    torch.cuda.synchronize()
+    assert not torch.any(dwr) and not torch.any(dwgu) and not torch.any(dwd)
+    assert B.moe_get_device_status(ws) == 0

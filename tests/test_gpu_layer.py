@@ -216,3 +216,21 @@ def test_forward_group_limited(libmoe):
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     yr = O.forward_rows(clean, np64(x), ref, lambda e: (np64(wgu[e]), np64(wd[e])), cfg.E, cfg.S)
     assert out_err(np64(out)[clean], yr) < TOL_BF16
+
+
+def test_forward_no_tokens(libmoe):
+    # T = 0: token buffers may be NULL; counts and offsets are zero, the bias is unchanged
+    cfg = I.MoEConfig("empty", 0, 256, 16, 1, 2, 128, 0.02)
+    s = _shape(cfg)
+    wr = I.make_router(cfg, DEV)
+    wgu, wd = I.make_experts(cfg, DEV)
+    x = torch.empty(0, cfg.d, dtype=torch.bfloat16, device=DEV)
+    bias = torch.full((cfg.E,), 0.25, dtype=torch.float32, device=DEV)
+    ws = B.alloc_workspace(s)
+    out, idx, gate, counts = B.moe_forward(s, x, wr, bias, wgu, wd, gamma=0.001, update_bias=True, ws=ws)
+    _, _, c2, offsets = B.moe_route(s, x, wr, bias, ws=ws)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.d) and idx.shape == (0, cfg.k)
+    assert not torch.any(counts) and not torch.any(c2) and not torch.any(offsets)
+    assert torch.all(bias == 0.25)
+    assert B.moe_get_device_status(ws) == 0
