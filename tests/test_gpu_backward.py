@@ -155,3 +155,20 @@ def test_backward_no_tokens(libmoe):
     torch.cuda.synchronize()
     assert not torch.any(dwr) and not torch.any(dwgu) and not torch.any(dwd)
     assert B.moe_get_device_status(ws) == 0
+
+
+def test_backward_rejects_out_of_range_experts(libmoe):
+    # an expert index outside [0, E) is caught on the device (MOE_ERR_DEVICE), nothing is
+    # read or written out of bounds, and the workspace is usable again after the status read
+    cfg = CASES["tiny"]
+    s, x, wr, off, wgu, wd, dout, idx = _inputs(cfg)
+    bad = idx.clone()
+    bad[5, 1] = cfg.E
+    ws = B.alloc_backward_workspace(s)
+    B.moe_backward(s, x, wr, wgu, wd, bad, dout, logit_offset=off, ws=ws)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 7
+    assert B.moe_get_device_status(ws) == 0
+    B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 0
