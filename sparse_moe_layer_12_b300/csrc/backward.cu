@@ -111,9 +111,9 @@ __global__ void __launch_bounds__(1024)
 // experts, then the shared ones) owns rows [64 kb_start[g], 64 kb_start[g+1]) of the
 // row buffers, its n tokens first.  groups: the token-row GEMMs (chunks of <= 256
 // tokens), with tile prefix sums for gate/up (I in 256-feature pairs), dh (I in
-// 512-blocks) and dx_rows (d in 512-blocks).  groups_a / groups_b: dW_down (d rows in
-// chunks of 256, I columns in 512-blocks) and dW_gate_up (2I rows in chunks of 256, d
-// columns in 512-blocks), K = the group's 64-row blocks.
+// 512-blocks) and dx_rows (d in 512-blocks).  groups_a / groups_b: dW_down (I columns in
+// chunks of 256, d rows in 512-blocks) and dW_gate_up (d columns in chunks of 256, 2I rows
+// in 512-blocks), K = the group's 64-row blocks.
 __global__ void __launch_bounds__(512)
     bwd_schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int d, int I,
                         GroupInfo* __restrict__ groups, int* __restrict__ ts_gu, int* __restrict__ ts_dh,
@@ -140,22 +140,20 @@ __global__ void __launch_bounds__(512)
   gi.nchunks = (ntok + kChunkMax - 1) / kChunkMax;
   gi.csize = gi.nchunks ? (((ntok + gi.nchunks - 1) / gi.nchunks + 15) & ~15) : 16;
   gi.expert = g;
-  ga.n = d;
+  ga.n = I;
   ga.csize = kChunkMax;
-  ga.nchunks = (d + kChunkMax - 1) / kChunkMax;
-  ga.out_row0 = g * d;
-  gb.n = 2 * I;
+  ga.nchunks = (I + kChunkMax - 1) / kChunkMax;
+  gb.n = d;
   gb.csize = kChunkMax;
-  gb.nchunks = (2 * I + kChunkMax - 1) / kChunkMax;
-  gb.out_row0 = g * 2 * I;
+  gb.nchunks = (d + kChunkMax - 1) / kChunkMax;
   ga.expert = gb.expert = g;
   ga.pad0 = gb.pad0 = kb0;
   ga.pad1 = gb.pad1 = nkb;
   const int n_gu = live ? gi.nchunks * ((I + 255) / 256) : 0;
   const int n_dh = live ? gi.nchunks * ((I + 511) / 512) : 0;
   const int n_dx = live ? gi.nchunks * ((d + 511) / 512) : 0;
-  const int n_a = live ? ga.nchunks * ((I + 511) / 512) : 0;
-  const int n_b = live ? gb.nchunks * ((d + 511) / 512) : 0;
+  const int n_a = live ? ga.nchunks * ((d + 511) / 512) : 0;
+  const int n_b = live ? gb.nchunks * ((2 * I + 511) / 512) : 0;
   const int t_gu = block_exclusive_scan(n_gu, buf);
   const int t_dh = block_exclusive_scan(n_dh, buf);
   const int t_dx = block_exclusive_scan(n_dx, buf);
@@ -534,8 +532,8 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
 
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap m_wgu, m_xp, m_wd_mn, m_dyp, m_wgu_mn, m_dgu, m_h_mn, m_dyp_mn, m_xp_mn, m_dgu_mn;
-  // weight gradients: A = the columns' operand of dW (h for dW_down, x for dW_gate_up) as
-  // [1][kcap][M] with 64 x 64 boxes, B = the rows' operand (dy, [da du]) as [kcap][N]
+  // weight gradients: A = the rows' operand of dW (dy for dW_down, [da du] for dW_gate_up)
+  // as [1][kcap][M] with 64 x 64 boxes, B = the columns' operand (h, x) as [kcap][N]
   const uint64_t I2 = 2 * (uint64_t)s.I;
   if (!make_map_3d(&m_wgu, w_gate_up, bf, 2, s.d, I2, G, 64, 128)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_xp, xp, bf, 2, s.d, kcap, 64, kBoxRows)) return MOE_ERR_CUDA;
@@ -543,10 +541,10 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
   if (!make_map_2d(&m_dyp, dyp, bf, 2, s.d, kcap, 64, kBoxRows)) return MOE_ERR_CUDA;
   if (!make_map_3d(&m_wgu_mn, w_gate_up, bf, 2, s.d, I2, G, 64, 64)) return MOE_ERR_CUDA;
   if (!make_map_2d(&m_dgu, dgu, bf, 2, I2, kcap, 64, kBoxRows)) return MOE_ERR_CUDA;
-  if (!make_map_3d(&m_h_mn, h, bf, 2, s.I, kcap, 1, 64, 64)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_dyp_mn, dyp, bf, 2, s.d, kcap, 64, 64)) return MOE_ERR_CUDA;
-  if (!make_map_3d(&m_xp_mn, xp, bf, 2, s.d, kcap, 1, 64, 64)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_dgu_mn, dgu, bf, 2, I2, kcap, 64, 64)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_h_mn, h, bf, 2, s.I, kcap, 64, 64)) return MOE_ERR_CUDA;
+  if (!make_map_3d(&m_dyp_mn, dyp, bf, 2, s.d, kcap, 1, 64, 64)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_xp_mn, xp, bf, 2, s.d, kcap, 64, 64)) return MOE_ERR_CUDA;
+  if (!make_map_3d(&m_dgu_mn, dgu, bf, 2, I2, kcap, 1, 64, 64)) return MOE_ERR_CUDA;
 
   // 3 [a | u] (FP32), h; dh (FP32)
   MOE_RC(launch_gemm_bwd(GemmMode::kGateUpRaw, m_wgu, m_xp, m_xp, groups, ts_gu, G, s.E, s.d, s.I, s.d, au, h, status,
@@ -569,12 +567,13 @@ moe_status_t launch_backward(const moe_shape_t& s, const void* x, const void* w_
                                                                        groups, s.d, dw_router);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 7 weight gradients
-  CUtensorMap m_dwd, m_dwgu;  // outputs, stored from 32 x 128 staged tiles
-  if (!make_map_2d_plain(&m_dwd, dw_down, bf, 2, s.I, (uint64_t)G * s.d, 128, 32)) return MOE_ERR_CUDA;
-  if (!make_map_2d_plain(&m_dwgu, dw_gate_up, bf, 2, s.d, (uint64_t)G * I2, 128, 32)) return MOE_ERR_CUDA;
-  MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_h_mn, m_dyp_mn, m_dyp_mn, ga, ts_a, G, s.E, (int)kcap, s.I, s.I, dw_down,
+  CUtensorMap m_dwd, m_dwgu;  // outputs [G][rows][cols], stored from staged 128 x 32 tiles
+  if (!make_map_3d_sw64(&m_dwd, dw_down, bf, 2, s.I, s.d, G, 32, 128)) return MOE_ERR_CUDA;
+  if (!make_map_3d_sw64(&m_dwgu, dw_gate_up, bf, 2, s.d, I2, G, 32, 128)) return MOE_ERR_CUDA;
+  // (the `I` argument carries the output rows per expert, `width` its columns)
+  MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_dyp_mn, m_h_mn, m_h_mn, ga, ts_a, G, s.E, (int)kcap, s.d, s.I, dw_down,
                          nullptr, status, st, &m_dwd));
-  MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_xp_mn, m_dgu_mn, m_dgu_mn, gb, ts_b, G, s.E, (int)kcap, s.I, s.d,
+  MOE_RC(launch_gemm_bwd(GemmMode::kWgrad, m_dgu_mn, m_xp_mn, m_xp_mn, gb, ts_b, G, s.E, (int)kcap, 2 * s.I, s.d,
                          dw_gate_up, nullptr, status, st, &m_dwgu));
   return MOE_OK;
 }

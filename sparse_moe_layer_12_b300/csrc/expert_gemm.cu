@@ -73,8 +73,9 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStage + kStgBytes + kCtrl;
 //             rows at in_row0 (K-major), out = B A (width `d`)
 // kWgrad      A = rows [K][M] of one buffer (map_w [1][rows][M], MN-major), B = rows
 //             [K][N] of another (map_b0 [rows][N], MN-major), K = the group's 64-row
-//             blocks [pad0, pad0 + pad1); out[g] = B^T A: row = N index (chunks of
-//             256), col = M index (512 per tile, width `d`).  K is short (one
+//             blocks [pad0, pad0 + pad1); out[g] = A^T B: row = M index (512 per tile,
+//             `I` rows per group), col = N index (chunks of 256).  A TMEM lane holds
+//             one output row, so each thread stages 64 contiguous bytes per chunk.  K is short (one
 //             expert's tokens), so the output (the largest write of the backward)
 //             leaves through TMA stores (map_xg = the output map) of double-buffered
 //             staging tiles, and the epilogue is no longer the long pole.  (A ring of
@@ -134,7 +135,7 @@ __device__ __forceinline__ bool decode_tile(const GroupInfo* __restrict__ groups
 
 // GATHER (gate/up only): routed token rows are gathered from x (map_xg: [x_rows, K]
 // bf16, box 64 x 1 row) through perm_token instead of read from map_b0.  kWgrad:
-// map_xg is the output map (no swizzle, box 128 x 32).
+// map_xg is the output map ([G][rows][cols], 64-byte swizzle, box 32 x 128).
 template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
@@ -418,18 +419,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             continue;
           }
           if (MODE == kWgrad) {
-            uint16_t* sb = stg + (grp * 2 + (spass & 1)) * (32 * 128);
+            // this thread's output row (TMEM lane f), output columns tok0 + c0 .. + 31:
+            // 64 bytes staged in a [128 rows][32 columns] tile with the 64-byte swizzle
+            // (16-byte chunk c of row f at c ^ ((f >> 1) & 3)), then one TMA store
+            uint8_t* sb = reinterpret_cast<uint8_t*>(stg) + (grp * 2 + (spass & 1)) * 8192;
             if (etid == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
             named_bar_sync(1 + grp, 128);
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              sb[i * 128 + f] = __bfloat16_as_ushort(
-                  __float2bfloat16_rn(zero ? 0.0f : __uint_as_float(pass == 0 ? ra[i] : rb[i])));
+            for (int j = 0; j < 16; ++j)
+              pk[j] = zero ? 0u
+                           : pack_bf16x2(__uint_as_float(pass == 0 ? ra[2 * j] : rb[2 * j]),
+                                         __uint_as_float(pass == 0 ? ra[2 * j + 1] : rb[2 * j + 1]));
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(sb + f * 64 + ((c ^ ((f >> 1) & 3)) * 16)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             fence_proxy_async_smem();
             named_bar_sync(1 + grp, 128);
             if (etid == 0) {
-              const int col = ti.mp * 512 + pass * 256 + rank * 128;
-              if (col < d) tma_store_2d(&map_xg, sb, col, ti.out_row0 + c0);
+              const int mrow = ti.mp * 512 + pass * 256 + rank * 128;
+              if (mrow < I) tma_store_3d(&map_xg, sb, ti.tok0 + c0, mrow, ti.g);
               bulk_commit();  // one group per pass, empty when nothing was stored
             }
             ++spass;

@@ -90,6 +90,9 @@ moe_status_t cuda_status(cudaError_t e);
 // TMA descriptors (128-byte swizzle, zero fill out of bounds)
 bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                  uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+// 3-D map with 64-byte swizzle (box rows of 64 bytes; TMA stores of staged tiles)
+bool make_map_3d_sw64(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                      uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
 // the same without swizzle (row-major boxes in shared memory; TMA stores of staged tiles)
 bool make_map_2d_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                        uint64_t outer, uint32_t box_inner, uint32_t box_outer);
@@ -124,11 +127,11 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 //               [G][2I][K] (box 64 x 128), B rows map_b0 / map_b1 at in_row0 (box 64 x 32)
 //   kDgrad      out = B W[g] (width `width`); map_w [G][K][width] (box 64 x 64, read
 //               MN-major), B = map_b0 rows at in_row0 (box 64 x 32)
-//   kWgrad      out[g] = B^T A over the group's rows [64 pad0, 64 (pad0 + pad1)):
+//   kWgrad      out[g] = A^T B over the group's rows [64 pad0, 64 (pad0 + pad1)):
 //               map_w [1][rows][M] and map_b0 [rows][N] (boxes 64 x 64, MN-major);
-//               out row out_row0 + (N index, chunks of 256), col = M index (width
-//               `width`, 512 per tile), written by TMA stores through map_out
-//               ([rows of all groups][width], no swizzle, box 128 x 32)
+//               out[g][M index][N index] (M: 512 per tile, `I` per group; N: chunks of
+//               256), written by TMA stores through map_out ([G][I][N], 64-byte
+//               swizzle, box 32 x 128)
 //   kDgrad32    as kDgrad, out = FP32 rows
 enum class GemmMode : int { kGateUpRaw, kDgrad, kWgrad, kDgrad32 };
 moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUtensorMap& map_b0,
