@@ -172,3 +172,22 @@ def test_backward_rejects_out_of_range_experts(libmoe):
     B.moe_backward(s, x, wr, wgu, wd, idx, dout, logit_offset=off, ws=ws)
     torch.cuda.synchronize()
     assert B.moe_get_device_status(ws) == 0
+
+
+def test_forward_and_backward_at_the_largest_k_and_s(libmoe):
+    # k = 16 of 32 routed experts and S = 8 shared experts (the library's limits)
+    cfg = I.MoEConfig("maxks", 64, 256, 32, 8, 16, 128, 0.05, seed=21)
+    s, x, wr, off, wgu, wd, dout, idx = _inputs(cfg)
+    b = torch.zeros(cfg.E, dtype=torch.float32, device=DEV)
+    out, fidx, gate, counts = B.moe_forward(s, x, wr, b, wgu, wd)
+    (dx, dwr, dwgu, dwd), _ = _run(s, x, wr, off, wgu, wd, dout, idx)
+    torch.cuda.synchronize()
+    from oracle import moe_oracle as O
+    ref_f = O.forward(np64(x), np64(wr), np.zeros(cfg.E, np.float32), np64(wgu), np64(wd), cfg.k, cfg.S)
+    r = ref_f["route"]
+    clean = ~(r["boundary_tie"] | r["order_tie"])
+    assert np.array_equal(fidx.cpu().numpy()[clean], r["idx"][clean])
+    assert out_err(np64(out)[clean], ref_f["out"][clean]) < 2e-2
+    ref = BW.backward(np64(x), np64(wr), np64(wgu), np64(wd), idx.cpu().numpy(), np64(dout), cfg.S)
+    for n, g in (("dx", dx), ("dw_router", dwr), ("dw_gate_up", dwgu), ("dw_down", dwd)):
+        assert out_err(g, ref[n]) < TOL[n] and fro_err(g, ref[n]) < TOL_FRO, n
