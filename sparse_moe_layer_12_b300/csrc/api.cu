@@ -174,19 +174,6 @@ bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map_2d_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
-                       uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn f = encode_fn();
-  if (!f || !aligned16(base)) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * (uint64_t)esize};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return f(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_map_3d_sw64(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                       uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid) {
   EncodeTiledFn f = encode_fn();

@@ -93,9 +93,6 @@ bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
 // 3-D map with 64-byte swizzle (box rows of 64 bytes; TMA stores of staged tiles)
 bool make_map_3d_sw64(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                       uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
-// the same without swizzle (row-major boxes in shared memory; TMA stores of staged tiles)
-bool make_map_2d_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
-                       uint64_t outer, uint32_t box_inner, uint32_t box_outer);
 bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                  uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
 
