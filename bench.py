@@ -63,6 +63,18 @@ def _config(args):
     return cfg
 
 
+L2_BYTES = 126 * 2**20  # B300 L2
+
+
+def _l2_note(cfg) -> str:
+    """What keeps the timed steps from running out of L2: the expert weights streamed
+    every step are larger than L2 for every workload but the tiny correctness one."""
+    wbytes = (cfg.E + cfg.S) * 3 * cfg.d * cfg.I * (1 if cfg.fp8 else 2)
+    if wbytes > L2_BYTES:
+        return "inputs larger than L2 (expert weights streamed every step)"
+    return "inputs smaller than L2 and no flush (tiny correctness workload, not a performance line)"
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -257,7 +269,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": f"{cfg.name} T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} k={cfg.k} "
-                                                    f"I={cfg.I}", "l2": "inputs larger than L2"},
+                                                    f"I={cfg.I}", "l2": _l2_note(cfg)},
         "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v,
                          "unit": "tokens/s"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -566,7 +578,7 @@ def run_ours(args):
         "data": "synthetic (seeded, random-init weights of the layer's shape)",
         "config": {"workload": f"{cfg.name}: T={cfg.T}/GPU d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}",
                    "global_batch": world * cfg.T, "parallelism": f"dp{world} (token-sharded replicas)",
-                   "l2": "inputs larger than L2 (expert weights streamed every step)"},
+                   "l2": _l2_note(cfg)},
         "expert_gemm_tflops": achieved,
         "expert_gemm_pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline,
