@@ -23,7 +23,9 @@ one float32 division; the dequantised value is decode(code) * scale.
 
 parity: pinned by tests/test_oracle_fp8.py (every one of the 256 codes against
 torch.float8_e4m3fn, random casts against torch, saturation and subnormal
-closed forms, per-tile scale invariants).
+closed forms, per-tile scale invariants; the quantisation of h inside the FP8
+expert by a hand-derived case in which it is the only rounding, so that leaving
+h unquantised, or tiling it along tokens or per whole row, fails).
 """
 from __future__ import annotations
 

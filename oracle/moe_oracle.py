@@ -37,7 +37,8 @@ other product is float64.
 
 parity: pinned by tests/test_oracle_*.py (hand-worked 4x4 example in
 tests/golden, brute-force top-k, invariants, reduction to a plain SwiGLU FFN,
-dense-mixture special case, closed-form bias update).
+dense-mixture special case, closed-form bias update, a hand-worked combine and
+the combine of permuted expert rows against the layer forward).
 """
 from __future__ import annotations
 

@@ -105,3 +105,42 @@ def test_forward_rows_matches_forward_on_subset():
     rows = np.array([0, 7, 13, 39])
     sub = O.forward_rows(rows, x, full["route"], lambda e: (wgu[e], wd[e]), E, S)
     np.testing.assert_allclose(sub, full["out"][rows], rtol=1e-12, atol=1e-12)
+
+
+def test_combine_hand_worked():
+    # T = 2 tokens, k = 2 slots, S = 2 shared experts, d = 2.  Routed rows 0..3, then
+    # shared expert 0 on tokens 0, 1 (rows 4, 5), shared expert 1 (rows 6, 7).
+    y = np.array([[1, 0], [0, 1], [10, 0], [0, 10],
+                  [100, 100], [200, 200],
+                  [1000, 0], [0, 1000]], dtype=np.float64)
+    gate = np.array([[0.75, 0.25], [0.6, 0.4]])
+    inv_pos = np.array([[2, 0], [1, 3]])
+    # token 0: 100 + 1000 (shared) + 0.75 * row 2 + 0.25 * row 0 = [1107.75, 100]
+    # token 1: 200 + 1000 (shared) + 0.6 * row 1 + 0.4 * row 3   = [200, 1204.6]
+    want = np.array([[1107.75, 100.0], [200.0, 1204.6]])
+    got = O.combine(y, gate, inv_pos, T=2, k=2, S=2)
+    np.testing.assert_allclose(got, want, rtol=1e-15, atol=1e-12)
+
+
+def test_combine_of_permuted_expert_rows_is_the_layer():
+    # the routed rows in permuted order (expert-major, tokens ascending) followed by the
+    # shared rows, combined through inv_pos, give the layer output of forward()
+    rng = np.random.default_rng(4)
+    T, d, I, E, S, k = 23, 16, 8, 6, 2, 3
+    x = _rand(rng, T, d)
+    wr = _rand(rng, E, d, scale=0.5)
+    wgu = _rand(rng, E + S, 2 * I, d, scale=d ** -0.5)
+    wd = _rand(rng, E + S, d, I, scale=I ** -0.5)
+    b = _rand(rng, E, scale=0.05)
+    res = O.forward(x, wr, b, wgu, wd, k=k, S=S)
+    r = res["route"]
+    p = O.permutation(r["idx"], E)
+    y = np.zeros((T * k + S * T, d))
+    for e in range(E):
+        lo, hi = p["offsets"][e], p["offsets"][e + 1]
+        if hi > lo:
+            y[lo:hi] = O.swiglu_expert(x[p["perm_token"][lo:hi]], wgu[e], wd[e])
+    for s_id in range(S):
+        y[T * k + s_id * T: T * k + (s_id + 1) * T] = O.swiglu_expert(x, wgu[E + s_id], wd[E + s_id])
+    got = O.combine(y, r["gate"], p["inv_pos"], T, k, S)
+    np.testing.assert_allclose(got, res["out"], rtol=1e-12, atol=1e-12)

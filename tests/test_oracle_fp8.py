@@ -105,3 +105,79 @@ def test_fp8_expert_close_to_unquantised():
     rms_err = np.sqrt(np.mean((y8 - y) ** 2) / np.mean(y ** 2))
     assert 5e-3 < rms_err < 8e-2
     assert O.max_rel_err(y8, y) < 0.5
+
+
+# ---- h quantisation inside the FP8 expert, pinned by hand-derived codes.
+# x and every weight are exact in E4M3 with power-of-two scales, so the only
+# rounding in the expert is the 1x128 quantisation of h along I ("DeepSeek-V3 详解"
+# 4.2: activations scaled per 1x128 tile along the contraction dimension).  Every
+# gate row is the same, so inside a token all a_i are equal and h_i / amax(tile)
+# = u_i / max|u| over the tile: 448 * u_i / max|u| lands on a code picked by hand
+# (each far from a midpoint between two codes), whatever the exact value of silu(a).
+
+# tile 0 of I: up values (x 0.25 * x0) and the code 448 * v / 1.25 rounds to
+_H_TILE0 = {1.25: 448.0, 1.0: 352.0, 0.875: 320.0, 0.5: 176.0, -0.75: -256.0, 0.0: 0.0, 0.0625: 22.0}
+# tile 1 of I: amax 3.0 (not a power-of-two multiple of tile 0's, so a per-row
+# scale would round tile 0 differently)
+_H_TILE1 = {3.0: 448.0, 2.5: 384.0, -1.75: -256.0, 1.0: 144.0}
+
+
+def _e4m3_codes(v):
+    return torch.tensor(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _h_quant_case():
+    d, I = 128, 256
+    up = np.zeros(I)
+    t0, t1 = list(_H_TILE0), list(_H_TILE1)
+    for i in range(128):
+        up[i] = t0[i % len(t0)]
+        up[128 + i] = t1[i % len(t1)]
+    # gate/up weight [2I, d]: only column 0 is non-zero; gate rows 1.0, up rows `up`;
+    # every 128x128 block has scale 0.25
+    w = np.zeros((2 * I, d))
+    w[:I, 0] = 1.0
+    w[I:, 0] = up
+    wgu_q, wgu_sc = _e4m3_codes(w), np.full((2 * I // 128, 1), 0.25, np.float32)
+    # down weight [d, I]: y_j = h_j + h_{128+j} (codes of 1.0, block scales 1.0)
+    wd = np.zeros((d, I))
+    wd[np.arange(128), np.arange(128)] = 1.0
+    wd[np.arange(128), 128 + np.arange(128)] = 1.0
+    wd_q, wd_sc = _e4m3_codes(wd), np.ones((1, 2), np.float32)
+    # two tokens, x = x0 * e_0 with x0 = 1.75 and 3.5: amax / 448 = 2^-8 and 2^-7, exact
+    x0 = np.array([1.75, 3.5])
+    x = np.zeros((2, d), np.float32)
+    x[:, 0] = x0
+    return x, x0, up, wgu_q, wgu_sc, wd_q, wd_sc
+
+
+def test_fp8_expert_quantises_h_per_1x128_along_I():
+    x, x0, up, wgu_q, wgu_sc, wd_q, wd_sc = _h_quant_case()
+    y = Q.fp8_swiglu_expert(x, wgu_q, wgu_sc, wd_q, wd_sc)
+    for t in range(2):
+        a = 0.25 * x0[t]  # gate: code 1.0 x block scale 0.25 x x0
+        silu_a = float(torch.nn.functional.silu(torch.tensor(a, dtype=torch.float64)))
+        hq = np.zeros(256)
+        for tile, table, vmax in ((0, _H_TILE0, 1.25), (1, _H_TILE1, 3.0)):
+            # h_i = silu(a) * 0.25 * x0 * up_i; the tile's scale is its amax / 448
+            scale = silu_a * 0.25 * x0[t] * vmax / 448.0
+            for i in range(tile * 128, tile * 128 + 128):
+                hq[i] = table[up[i]] * scale
+        want = hq[:128] + hq[128:]
+        # float32 rounding of h and of the scale is the only slack left
+        np.testing.assert_allclose(y[t], want, rtol=1e-6, atol=0)
+
+
+def test_fp8_expert_h_rounding_is_visible():
+    # the same case without any quantisation of h differs by far more than the pin's
+    # tolerance, so the pin above cannot pass with h left unquantised
+    x, x0, up, wgu_q, wgu_sc, wd_q, wd_sc = _h_quant_case()
+    y = Q.fp8_swiglu_expert(x, wgu_q, wgu_sc, wd_q, wd_sc)
+    wgu = Q.dequant_weight(wgu_q, wgu_sc)
+    wd = Q.dequant_weight(wd_q, wd_sc)
+    a = x.astype(np.float64) @ wgu[:256].T
+    u = x.astype(np.float64) @ wgu[256:].T
+    h = torch.nn.functional.silu(torch.from_numpy(a)).numpy() * u
+    y_exact_h = h @ wd.T
+    rel = np.abs(y - y_exact_h) / np.maximum(np.abs(y_exact_h), 1e-30)
+    assert rel.max() > 1e-2
