@@ -174,10 +174,16 @@ MOE_API moe_status_t moe_expert_ffn_gather(const moe_shape_t* shape, const void*
                                            const float* w_down_scale, void* y, void* ws, size_t ws_bytes,
                                            moe_stream_t stream);
 
-/* Combine: out[t] = sum_s y[T*k + s*T + t] + sum_j topk_gate[t, j] * y[inv_pos[t, j]]
+/* Combine: the layer output of each token is its shared experts' outputs, ungated,
+ * plus its k routed experts' outputs weighted by their gates ("deepseek-v3-report",
+ * model table: 8 routed + 1 shared experts per token; "拆解DeepSeek V3", section
+ * "让256个专家都干活": the shared expert serves every token; the single-GPU form of
+ * the all-to-all combine in "DeepSeek-V3 Overview and Key Innovations", Training
+ * Infrastructure and Optimization):
+ *     out[t] = sum_s y[T*k + s*T + t] + sum_j topk_gate[t, j] * y[inv_pos[t, j]]
  * (shared experts first, then slots j = 0..k-1, FP32 sum, bf16 store).
  *   y bf16 [T*k + S*T, d]; topk_gate f32 [T, k]; inv_pos int32 [T, k];
- *   out bf16 [T, d] (out). */
+ *   out bf16 [T, d] (out).  Deterministic run to run. */
 MOE_API moe_status_t moe_combine(const moe_shape_t* shape, const void* y, const float* topk_gate,
                          const int32_t* inv_pos, void* out, moe_stream_t stream);
 
@@ -189,7 +195,11 @@ MOE_API moe_status_t moe_bias_update(const moe_shape_t* shape, const int32_t* co
 
 /* The whole layer: moe_route, the dispatch, the expert FFN, moe_combine and,
  * when update_bias != 0, moe_bias_update with this batch's counts (after the
- * routing has used the old bias).  topk_idx, topk_gate and counts are optional
+ * routing has used the old bias).  This is the MoE layer of "DeepSeek-V3 详解"
+ * 2.2-2.3 (fine-grained routed experts plus a shared expert, selection by the
+ * biased score, the bias moved after each step) with the sizes of
+ * "DeepSeek-V3 技术报告要点" section 3, and the per-batch bias update of its
+ * section 4.2.  topk_idx, topk_gate and counts are optional
  * outputs (NULL keeps them in the workspace).  All intermediates live in `ws`.
  * The dispatch takes one of two forms (moe_forward_gathers tells which; both
  * give bit-identical results): for batches with T*k <= 4096 moe_permute builds
@@ -213,21 +223,30 @@ MOE_API int moe_forward_gathers(const moe_shape_t* shape);
  * owns all device memory and offers no workspace, or a serving loop that
  * forbids cudaMalloc after start-up.  The paper has no counterpart; this is a
  * deployment convenience of the library.
- *   - Scratch (status word, schedule, SwiGLU intermediate h) comes from one
- *     64 MiB array compiled into the library, held on every GPU that loads
- *     the library until the process exits.  Layers needing more scratch are
- *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (T=256 at
- *     d=7168, 256+1 experts, top-8, I=2048 needs about 39 MB).
+ *   - Scratch (status word, schedule, the E4M3 copy of x on the FP8 path, the
+ *     SwiGLU intermediate h) comes from one 64 MiB array compiled into the
+ *     library, held on every GPU that loads the library until the process
+ *     exits.  Layers needing more scratch are rejected with MOE_ERR_WORKSPACE
+ *     before anything is enqueued; at d=7168, 256+1 experts, top-8, I=2048 the
+ *     scratch is about 36 KB per token in bf16 (up to about 1800 tokens) and
+ *     26 KB per token in FP8 (up to about 2500 tokens).
  *   - The first call on a device looks up the array's address; make that call
  *     before any stream capture.
  *   - All calls share the array; overlapping calls on the GPU race and give
- *     wrong results.  The status word is cleared at the start of each call.
+ *     wrong results.  The status word is cleared at the start of each call;
+ *     read it with moe_get_static_device_status.
  *   - Allocates nothing (no cudaMalloc / cudaFree). */
 MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, const void* x_perm,
                                            const float* x_perm_scale, const void* x,
                                            const int32_t* offsets, const void* w_gate_up,
                                            const float* w_gu_scale, const void* w_down,
                                            const float* w_down_scale, void* y, moe_stream_t stream);
+
+/* Reads (synchronising `stream`) and clears the device status word of the array
+ * that moe_expert_ffn_static uses on the current device, as moe_get_device_status
+ * does for a workspace: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (MOE_ERR_CUDA if
+ * the read fails).  The paper has no counterpart. */
+MOE_API moe_status_t moe_get_static_device_status(moe_stream_t stream);
 
 /* FP8 weight preparation ("DeepSeek-V3 详解" 4.2): quantise `w` bf16
  * [G, N, K] (N % 128 == 0, K % 128 == 0) per 128x128 block to E4M3 `w_q`

@@ -111,12 +111,15 @@ def route(x, w_router, bias, k, logit_offset=None, n_group=0, topk_group=0) -> d
       idx   int32 [T, k]  chosen experts, descending biased score, ties -> lower index
       gate  float64 [T, k] s[t, idx] / sum_j s[t, idx_j]
       s     float32 [T, E] affinities;  v float32 [T, E] biased scores s + b
+            (-inf outside the kept groups under group-limited routing)
+      v_all float32 [T, E] biased scores s + b of every expert
       boundary_tie bool [T]: k-th and (k+1)-th biased scores within NEAR_TIE
       order_tie    bool [T]: two adjacent chosen scores within NEAR_TIE
     """
     z = router_logits(x, w_router, logit_offset)
     s = affinity(z)
     v = s + np.asarray(bias, dtype=np.float32)[None, :]
+    v_all = v
     T, E = v.shape
     group_tie = np.zeros(T, dtype=bool)
     if n_group:
@@ -135,8 +138,8 @@ def route(x, w_router, bias, k, logit_offset=None, n_group=0, topk_group=0) -> d
         order_tie = (np.diff(-v_sorted[:, :k], axis=1) < NEAR_TIE).any(axis=1)
     else:
         order_tie = np.zeros(T, dtype=bool)
-    return dict(idx=idx, gate=gate, s=s, v=v, z=z, boundary_tie=boundary_tie | group_tie, order_tie=order_tie,
-                group_tie=group_tie)
+    return dict(idx=idx, gate=gate, s=s, v=v, v_all=v_all, z=z, boundary_tie=boundary_tie | group_tie,
+                order_tie=order_tie, group_tie=group_tie)
 
 
 def expert_counts(idx, E) -> np.ndarray:

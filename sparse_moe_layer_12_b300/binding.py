@@ -23,7 +23,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
            "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static",
-           "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward"]
+           "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward",
+           "moe_get_static_device_status"]
 
 
 class MoEError(RuntimeError):
@@ -58,6 +59,7 @@ _SIGS = {
     "moe_backward_workspace_bytes": (_SZ, [ctypes.POINTER(Shape)]),
     "moe_backward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_device_status": (_I, [_P, _P]),
+    "moe_get_static_device_status": (_I, [_P]),
     "moe_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_version": (ctypes.c_char_p, []),
@@ -231,7 +233,7 @@ def moe_expert_ffn_gather(shape: Shape, x, perm_token, offsets, w_gate_up, w_dow
 
 
 def moe_expert_ffn_static(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_down, w_gu_scale=None,
-                          w_down_scale=None):
+                          w_down_scale=None, y=None):
     """moe_expert_ffn without a workspace: the library's fixed scratch array is used
     (for callers that cannot allocate device memory; one call at a time)."""
     T, d, E, S, k, I = shape.T, shape.d, shape.E, shape.S, shape.k, shape.I
@@ -241,7 +243,14 @@ def moe_expert_ffn_static(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
     _need(w_down, wdt, (E + S, d, I), "w_down")
-    y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    if shape.dtype == MOE_FP8_E4M3:
+        _need(x_perm_scale, torch.float32, (T * k, d // 128), "x_perm_scale")
+        _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
+        _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
+    if y is None:
+        y = torch.empty(T * k + S * T, d, dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, torch.bfloat16, (T * k + S * T, d), "y")
     _check("moe_expert_ffn_static", load().moe_expert_ffn_static(
         ctypes.byref(shape), _ptr(x_perm), _ptr(x_perm_scale), _ptr(x), _ptr(offsets), _ptr(w_gate_up),
         _ptr(w_gu_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y), _stream()))
@@ -354,6 +363,11 @@ def moe_backward(shape: Shape, x, w_router, w_gate_up, w_down, topk_idx, dout, l
 
 def moe_get_device_status(ws) -> int:
     return int(load().moe_get_device_status(_ptr(ws), _stream()))
+
+
+def moe_get_static_device_status() -> int:
+    """Reads and clears the status word of moe_expert_ffn_static's array on the current device."""
+    return int(load().moe_get_static_device_status(_stream()))
 
 
 def moe_debug_wait_timeout(ws, limit_us: int):

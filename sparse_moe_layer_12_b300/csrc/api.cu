@@ -73,6 +73,22 @@ WsLayout ws_layout(const moe_shape_t& s) {
   return L;
 }
 
+WsLayout ffn_ws_layout(const moe_shape_t& s) {
+  WsLayout L{};
+  const size_t A = 1024;
+  const size_t rows = (size_t)s.T * s.k + (size_t)s.S * s.T;
+  const bool f8 = s.dtype == MOE_FP8_E4M3;
+  size_t o = 0;
+  L.status = o;      o = align_up(o + 256, A);
+  L.sched = o;       o = align_up(o + Schedule::bytes(s.E + s.S), A);
+  L.xq = o;          o = align_up(o + (f8 ? (size_t)s.T * s.d : 0), A);
+  L.xq_scale = o;    o = align_up(o + (f8 ? (size_t)s.T * (s.d / 128) * 4 : 0), A);
+  L.h = o;           o = align_up(o + rows * s.I * (f8 ? 1 : 2), A);
+  L.h_scale = o;     o = align_up(o + (f8 ? rows * (s.I / 128) * 4 : 0), A);
+  L.total = o;
+  return L;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // a buffer with one entry per token (or per routed row) may be NULL when there are no tokens

@@ -7,21 +7,26 @@
 // start-up (cudaMalloc may synchronise the device and fragments the framework's
 // pool).  For them this entry point runs the same grouped expert GEMMs as
 // moe_expert_ffn, but takes its scratch (the device status word, the expert-GEMM
-// schedule and the SwiGLU intermediate h) from a fixed array compiled into the
-// library instead of a caller-provided workspace.
+// schedule, the E4M3 copy of x on the FP8 path and the SwiGLU intermediate h)
+// from a fixed array compiled into the library instead of a caller-provided
+// workspace, packed tighter than the workspace layout (which also holds what
+// moe_forward needs).
 //
 //   * The array is kStaticScratchBytes (64 MiB).  Every GPU that loads the
 //     library holds it until the process exits.
 //   * Layers whose scratch does not fit are rejected with MOE_ERR_WORKSPACE
-//     before anything is enqueued (decode-sized batches fit: e.g. T=256 tokens
-//     at d=7168, 256+1 experts, top-8, I=2048 needs about 39 MB).
+//     before anything is enqueued.  At d=7168, 256+1 experts, top-8, I=2048 the
+//     scratch is about 36 KB per token in bf16 (up to 1800 tokens) and 26 KB per
+//     token in FP8 (up to 2500 tokens).
 //   * The first call on a device looks up the array's device address (one
 //     cudaGetSymbolAddress with that device current); make that first call
 //     before any stream capture.
 //   * All calls share the one array, which keeps the last call's contents.  The
-//     status word is cleared at the start of every call.  Calls that overlap on
-//     the GPU (different streams, or different host threads, without ordering
-//     between them) race on the array and give wrong results.
+//     status word is cleared at the start of every call; an error found on the
+//     device (inconsistent offsets, a wait that gave up) is read back with
+//     moe_get_static_device_status before the next call clears it.  Calls that
+//     overlap on the GPU (different streams, or different host threads, without
+//     ordering between them) race on the array and give wrong results.
 //   * Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
 //     routine.
 #include <mutex>
@@ -56,15 +61,6 @@ moe_status_t scratch_address(void** out) {
   return MOE_OK;
 }
 
-// Highest workspace byte the expert FFN touches (status word, schedule, FP8
-// copies of x, h and its scales): everything up to the end of h / h_scale.
-size_t ffn_scratch_bytes(const moe_shape_t& s) {
-  const moe::WsLayout L = moe::ws_layout(s);
-  const size_t rows = (size_t)s.T * s.k + (size_t)s.S * s.T;
-  if (s.dtype == MOE_FP8_E4M3) return L.h_scale + rows * (s.I / 128) * 4;
-  return L.h + rows * (size_t)s.I * 2;
-}
-
 }  // namespace
 
 extern "C" MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, const void* x_perm,
@@ -85,7 +81,8 @@ extern "C" MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, 
   if (!moe::aligned16(x_perm) || !moe::aligned16(x) || !moe::aligned16(w_gate_up) || !moe::aligned16(w_down) ||
       !moe::aligned16(y))
     return MOE_ERR_ALIGNMENT;
-  if (ffn_scratch_bytes(s) > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
+  const moe::WsLayout L = moe::ffn_ws_layout(s);
+  if (L.total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
   void* scratch = nullptr;
   const moe_status_t st = scratch_address(&scratch);
   if (st != MOE_OK) return st;
@@ -93,5 +90,14 @@ extern "C" MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, 
   // the device status word must start clear; the rest is overwritten before use
   if (cudaMemsetAsync(scratch, 0, 256, cs) != cudaSuccess) return MOE_ERR_CUDA;
   return moe::launch_expert_ffn(s, x_perm, x_perm_scale, x, nullptr, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
-                                y, scratch, cs);
+                                y, scratch, cs, &L);
+}
+
+// The status word of the static array on the current device: the same read-and-clear
+// as moe_get_device_status on a workspace.
+extern "C" MOE_API moe_status_t moe_get_static_device_status(moe_stream_t stream) {
+  void* scratch = nullptr;
+  const moe_status_t st = scratch_address(&scratch);
+  if (st != MOE_OK) return st;
+  return moe_get_device_status(scratch, stream);
 }

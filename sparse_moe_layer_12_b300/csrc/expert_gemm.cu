@@ -582,13 +582,13 @@ __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int 
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
                                const int32_t* perm_token, const int32_t* offsets, const void* w_gate_up,
                                const float* w_gu_scale, const void* w_down, const float* w_down_scale, void* y,
-                               void* ws, cudaStream_t st) {
+                               void* ws, cudaStream_t st, const WsLayout* layout) {
   if (s.T == 0) return MOE_OK;
   if (s.dtype == MOE_FP8_E4M3)
     return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, perm_token, offsets, w_gate_up, w_gu_scale, w_down,
-                                 w_down_scale, y, ws, st);
+                                 w_down_scale, y, ws, st, layout);
   const bool gather = perm_token != nullptr;
-  const WsLayout L = ws_layout(s);
+  const WsLayout L = layout ? *layout : ws_layout(s);
   char* w = static_cast<char*>(ws);
   const int G = s.E + s.S;
   GroupInfo* groups = reinterpret_cast<GroupInfo*>(w + L.sched);

@@ -424,9 +424,10 @@ __global__ void __launch_bounds__(128) quant_rows_kernel(const uint4* __restrict
 moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
                                    const void* x, const int32_t* perm_token, const int32_t* offsets,
                                    const void* w_gate_up, const float* w_gu_scale, const void* w_down,
-                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st) {
+                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st,
+                                   const WsLayout* layout) {
   const bool gather = perm_token != nullptr;
-  const WsLayout L = ws_layout(s);
+  const WsLayout L = layout ? *layout : ws_layout(s);
   char* w = static_cast<char*>(ws);
   const int G = s.E + s.S;
   GroupInfo* groups = reinterpret_cast<GroupInfo*>(w + L.sched);

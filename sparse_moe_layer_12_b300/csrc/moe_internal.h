@@ -73,6 +73,9 @@ BwdLayout bwd_layout(const moe_shape_t& s);
 bool shape_valid(const moe_shape_t* s);
 bool forward_gathers(const moe_shape_t& s);  // moe_forward's dispatch form (see moe_forward_gathers)
 WsLayout ws_layout(const moe_shape_t& s);
+// The expert FFN's scratch alone (status word, schedule, FP8 copy of x and its scales,
+// h and its scales), packed; the other fields are 0 and unused.  `total` is its size.
+WsLayout ffn_ws_layout(const moe_shape_t& s);
 
 // status word helpers (the word lives at offset 0 of the workspace)
 inline int* ws_status(void* ws) { return reinterpret_cast<int*>(ws); }
@@ -106,14 +109,18 @@ moe_status_t launch_permute(const moe_shape_t& s, const void* x, const int32_t* 
                             cudaStream_t st);
 // perm_token == nullptr: routed rows from x_perm (+ x_perm_scale); otherwise the
 // gate/up GEMM gathers them from x through perm_token and x_perm is unused
+// `layout` places the FFN's scratch inside `ws` (nullptr: ws_layout(s), the layout of
+// every call that takes a workspace)
 moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
                                const void* x, const int32_t* perm_token, const int32_t* offsets,
                                const void* w_gate_up, const float* w_gu_scale, const void* w_down,
-                               const float* w_down_scale, void* y, void* ws, cudaStream_t st);
+                               const float* w_down_scale, void* y, void* ws, cudaStream_t st,
+                               const WsLayout* layout = nullptr);
 moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale,
                                    const void* x, const int32_t* perm_token, const int32_t* offsets,
                                    const void* w_gate_up, const float* w_gu_scale, const void* w_down,
-                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st);
+                                   const float* w_down_scale, void* y, void* ws, cudaStream_t st,
+                                   const WsLayout* layout = nullptr);
 // per-group token counts, chunking (<= chunk_max tokens) and tile prefix sums (one block of 512 threads)
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
                                 int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,

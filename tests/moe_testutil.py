@@ -47,6 +47,23 @@ def check_routing(ref, idx, gate, counts, offsets, E, n_group=0, topk_group=0):
         assert np.all(v[t][idx[t]] >= kth - O.NEAR_TIE), t
         must = np.nonzero(v[t] > kth + O.NEAR_TIE)[0]
         assert set(must.tolist()) <= set(idx[t].tolist()), t
+    # 4. ties between kept and dropped groups: the groups used must be among the best
+    #    topk_group within 1e-5, every group clearly better than the first dropped one
+    #    must stay eligible, and no eligible expert left out may beat a chosen one
+    for t in np.nonzero(gtie)[0]:
+        assert len(set(idx[t].tolist())) == k, t
+        va = ref["v_all"][t].astype(np.float64)
+        m = -(-k // topk_group)
+        gs = np.sort(va.reshape(n_group, gsz), axis=1)[:, ::-1][:, :m].sum(1)
+        gsort = np.sort(gs)[::-1]
+        used = {e // gsz for e in idx[t].tolist()}
+        assert all(gs[g] >= gsort[topk_group - 1] - O.NEAR_TIE for g in used), t
+        kept = used | set(np.nonzero(gs > gsort[topk_group] + O.NEAR_TIE)[0].tolist())
+        weakest = va[idx[t]].min()
+        for g in kept:
+            for e in range(g * gsz, (g + 1) * gsz):
+                if e not in set(idx[t].tolist()):
+                    assert va[e] <= weakest + O.NEAR_TIE, (t, e)
     # gates: unbiased affinity of the chosen expert over the chosen sum
     s = ref["s"].astype(np.float64)
     s_sel = np.take_along_axis(s, idx.astype(np.int64), axis=1)
@@ -76,3 +93,17 @@ def out_err(out, ref) -> float:
     ref = np.asarray(ref, np.float64)
     rms = np.sqrt(np.mean(ref * ref))
     return float(np.max(np.maximum(np.abs(o - ref) - BF16_HALF_ULP * np.abs(ref), 0.0)) / rms)
+
+
+def fro_err(out, ref) -> float:
+    """Relative Frobenius (RMS-normalised) error ||out - ref|| / ||ref|| over the compared
+    elements: the bound a systematic error (a dropped term, a wrong index) cannot pass."""
+    o = np64(out) if isinstance(out, torch.Tensor) else np.asarray(out, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(o - ref) / np.linalg.norm(ref))
+
+
+def errs(out, ref) -> dict:
+    """The three error figures the parity tests print: the gated computation error beyond
+    bf16 storage rounding (out_err), the plain max/RMS and the relative Frobenius error."""
+    return dict(out_err=out_err(out, ref), max_rms=rel_err(out, ref), fro=fro_err(out, ref))

@@ -3,8 +3,11 @@ blocks, FP32 accumulation) against the oracle's FP8 layer.
 
 Codes and scales that both sides compute from the same bf16 inputs (x, weights)
 must match bit for bit.  Float outputs are compared with the oracle's FP8 layer
-under the same simulated quantisation, within 6e-2 of the output RMS (the
-computation error beyond the bf16 storage rounding, as for bf16)."""
+under the same simulated quantisation at the bf16 bounds (computation error beyond
+bf16 storage rounding <= 2e-2 of the output RMS, relative Frobenius error <= 5e-3),
+and with the same layer left unquantised (x and h exact) at a relative Frobenius
+error <= 6e-2: E4M3's three mantissa bits alone cost about 4.4 % there, and the
+max error against the unquantised layer (20-30 % of the RMS) is reported only."""
 import numpy as np
 import pytest
 import torch
@@ -13,11 +16,13 @@ from oracle import fp8 as Q
 from oracle import moe_oracle as O
 from sparse_moe_layer_12_b300 import binding as B
 from sparse_moe_layer_12_b300 import inputs as I
-from moe_testutil import check_routing, np64, oracle_route, out_err, rel_err
+from moe_testutil import check_routing, errs, np64, oracle_route
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL_FP8 = 6e-2
+TOL_MAX = 2e-2
+TOL_FRO = 5e-3
+TOL_FRO_UNQUANTISED = 6e-2
 
 
 def _u8(t):
@@ -82,31 +87,20 @@ def test_fp8_forward(libmoe, name):
     ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     tok = clean[:: max(1, cfg.T // 128)]
-    yr = Q.fp8_forward_rows(tok, np64(x), ref, _fp8_getter(wgu, gs, wd, ds), cfg.E, cfg.S)
-    err = out_err(np64(out)[tok], yr)
-    print(f"{name} fp8: err {err:.3e} (plain max/RMS {rel_err(np64(out)[tok], yr):.3e}), near ties {ties}")
-    assert err < TOL_FP8
+    get = _fp8_getter(wgu, gs, wd, ds)
+    yr = Q.fp8_forward_rows(tok, np64(x), ref, get, cfg.E, cfg.S)
+
+    def get_unq(e):
+        gq, gsc, dq, dsc = get(e)
+        return Q.dequant_weight(gq, gsc), Q.dequant_weight(dq, dsc)
+
+    yu = O.forward_rows(tok, np64(x), ref, get_unq, cfg.E, cfg.S)
+    o = np64(out)[tok]
+    e, eu = errs(o, yr), errs(o, yu)
+    print(f"{name} fp8 (near ties {ties}): vs the oracle's FP8 layer out_err {e['out_err']:.3e} "
+          f"max/RMS {e['max_rms']:.3e} Frobenius {e['fro']:.3e}; vs the unquantised layer "
+          f"max/RMS {eu['max_rms']:.3e} Frobenius {eu['fro']:.3e}")
+    assert e["out_err"] < TOL_MAX and e["fro"] < TOL_FRO
+    assert eu["fro"] < TOL_FRO_UNQUANTISED
     out2, *_ = B.moe_forward(s, x, wr, b.clone(), wgu, wd, w_gu_scale=gs, w_down_scale=ds, ws=ws)
     assert torch.equal(out, out2), "deterministic"
-
-
-def test_fp8_forward_v3_sampled(libmoe):
-    cfg = I.CONFIGS["v3fp8"]
-    x = I.make_x(cfg, DEV)
-    wr = I.make_router(cfg, DEV)
-    b = I.make_bias(cfg, DEV)
-    wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV)
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8=True)
-    ws = B.alloc_workspace(s)
-    out, idx, gate, counts = B.moe_forward(s, x, wr, b.clone(), wgu, wd, w_gu_scale=gs, w_down_scale=ds, ws=ws)
-    torch.cuda.synchronize()
-    assert B.moe_get_device_status(ws) == 0
-    ref = oracle_route(x, wr, b, cfg.k)
-    offsets = torch.tensor(O.offsets_from_counts(counts.cpu().numpy()))
-    ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
-    clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
-    tok = np.sort(np.random.default_rng(1).choice(clean, size=4, replace=False))
-    yr = Q.fp8_forward_rows(tok, np64(x), ref, _fp8_getter(wgu, gs, wd, ds), cfg.E, cfg.S)
-    err = out_err(np64(out)[tok], yr)
-    print(f"v3fp8: sampled err {err:.3e} (plain {rel_err(np64(out)[tok], yr):.3e}), near ties {ties}")
-    assert err < TOL_FP8

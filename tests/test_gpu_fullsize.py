@@ -1,0 +1,174 @@
+"""Parity at the full V3 sizes, in the launch configuration the benchmark times
+(moe_route, moe_permute with the permuted copy, moe_expert_ffn, moe_combine).
+
+Whole routed experts are compared element by element with the oracle -- every
+token row of the expert, so every row position of the 256-token tiles, every
+chunk boundary and every 256-feature block of its schedule is hit -- together
+with the shared expert on its first and last 256-token chunks, and the layer
+output on 256 tokens.  Two bounds per comparison: the computation error beyond
+bf16 storage rounding over the output RMS (max over elements), and the relative
+Frobenius error, which a dropped term or a wrong index cannot pass.
+
+bf16: out_err <= 2e-2, Frobenius <= 5e-3 (h, y and out are each rounded to bf16
+once: 2^-9 / sqrt(3) RMS relative error each, about 2e-3 together).
+FP8: against the oracle's FP8 layer (same 1x128 / 128x128 quantisation) the same
+bounds as bf16, since both sides quantise the same values; against the layer with
+x and h left unquantised the relative Frobenius error must stay below 6e-2 (E4M3's
+three mantissa bits alone cost about 4.4 %, and its max error, 20-30 % of the RMS,
+is reported only).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8 as Q
+from oracle import moe_oracle as O
+from sparse_moe_layer_12_b300 import binding as B
+from sparse_moe_layer_12_b300 import inputs as I
+from moe_testutil import check_routing, errs, np64, oracle_route
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_MAX = 2e-2
+TOL_FRO = 5e-3
+TOL_FRO_FP8_UNQUANTISED = 6e-2
+
+
+def _pick_experts(counts, rng):
+    """Four routed experts: the largest group, the smallest non-empty one, one of more
+    than 256 tokens whose size is not a multiple of 16 (a ragged tail after a full
+    chunk), and a random one."""
+    nz = np.nonzero(counts)[0]
+    picks = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])]
+    ragged = [e for e in nz if counts[e] > 256 and counts[e] % 16 and e not in picks]
+    if ragged:
+        picks.append(int(ragged[0]))
+    rest = [int(e) for e in rng.permutation(nz) if int(e) not in picks]
+    picks += rest[: 4 - len(picks)]
+    return picks
+
+
+def _shared_rows(T):
+    """Tokens of the shared expert's first and last 256-token chunks."""
+    return np.unique(np.concatenate([np.arange(min(256, T)), np.arange(max(0, T - 256), T)]))
+
+
+def _run_layer(cfg, x, wr, b, wgu, wd, gs=None, ds=None):
+    fp8 = gs is not None
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)
+    assert not B.forward_gathers(s), "the benchmark's dispatch form at this size is the permuted copy"
+    ws = B.alloc_workspace(s)
+    idx, gate, counts, offsets = B.moe_route(s, x, wr, b, ws=ws)
+    xp, xps, ptok, inv = B.moe_permute(s, x, idx, offsets, ws=ws)
+    y = B.moe_expert_ffn(s, xp, xps, x, offsets, wgu, wd, gs, ds, ws=ws)
+    out = B.moe_combine(s, y, gate, inv)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 0
+    # moe_forward runs the same kernels: the same bits
+    out_f, *_ = B.moe_forward(s, x, wr, b.clone(), wgu, wd, w_gu_scale=gs, w_down_scale=ds, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f, out)
+    return idx, gate, counts, offsets, ptok, y, out
+
+
+def _report(tag, e):
+    print(f"{tag}: out_err {e['out_err']:.3e}  max/RMS {e['max_rms']:.3e}  Frobenius {e['fro']:.3e}")
+
+
+def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, fro_tol=TOL_FRO):
+    xn = np64(x)
+    ptok = ptok.cpu().numpy()
+    off = offsets.cpu().numpy()
+    yg = y
+    for e in experts:
+        lo, hi = int(off[e]), int(off[e + 1])
+        want = expert_fn(e, xn[ptok[lo:hi]])
+        got = np64(yg[lo:hi])
+        r = errs(got, want)
+        _report(f"{cfg.name} expert {e} ({hi - lo} tokens)", r)
+        assert r["out_err"] < TOL_MAX and r["fro"] < fro_tol, e
+    Tk = cfg.T * cfg.k
+    tok = _shared_rows(cfg.T)
+    for si in range(cfg.S):
+        want = expert_fn(cfg.E + si, xn[tok])
+        got = np64(yg[torch.as_tensor(Tk + si * cfg.T + tok, device=yg.device)])
+        r = errs(got, want)
+        _report(f"{cfg.name} shared expert {si} ({tok.size} tokens)", r)
+        assert r["out_err"] < TOL_MAX and r["fro"] < fro_tol
+
+
+def _cached(fn):
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache.clear()
+            cache[e] = fn(e)
+        return cache[e]
+
+    return get
+
+
+def test_v3_bf16_whole_experts_and_output(libmoe):
+    cfg = I.CONFIGS["v3"]
+    x, wr, b = I.make_x(cfg, DEV), I.make_router(cfg, DEV), I.make_bias(cfg, DEV)
+    wgu, wd = I.make_experts(cfg, DEV)
+    idx, gate, counts, offsets, ptok, y, out = _run_layer(cfg, x, wr, b, wgu, wd)
+    ref = oracle_route(x, wr, b, cfg.k)
+    ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
+    print(f"v3: near-tied tokens {ties}")
+    get = _cached(lambda e: (np64(wgu[e]), np64(wd[e])))
+    experts = _pick_experts(counts.cpu().numpy(), np.random.default_rng(0))
+    _check_whole_experts(cfg, x, ptok, offsets, y, experts, lambda e, rows: O.swiglu_expert(rows, *get(e)))
+    clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
+    tok = np.sort(np.random.default_rng(1).choice(clean, size=256, replace=False))
+    yr = O.forward_rows(tok, np64(x), ref, get, cfg.E, cfg.S)
+    r = errs(np64(out)[tok], yr)
+    _report("v3 layer output (256 tokens)", r)
+    assert r["out_err"] < TOL_MAX and r["fro"] < TOL_FRO
+
+
+def test_v3_fp8_whole_experts_and_output(libmoe):
+    cfg = I.CONFIGS["v3fp8"]
+    x, wr, b = I.make_x(cfg, DEV), I.make_router(cfg, DEV), I.make_bias(cfg, DEV)
+    wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV)
+    idx, gate, counts, offsets, ptok, y, out = _run_layer(cfg, x, wr, b, wgu, wd, gs, ds)
+    ref = oracle_route(x, wr, b, cfg.k)
+    ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
+    print(f"v3fp8: near-tied tokens {ties}")
+
+    def u8(t):
+        return t.view(torch.uint8).cpu().numpy()
+
+    def load_q(e):
+        q = (u8(wgu[e]), gs[e].cpu().numpy(), u8(wd[e]), ds[e].cpu().numpy())
+        return q, Q.dequant_weight(q[0], q[1]), Q.dequant_weight(q[2], q[3])
+
+    getall = _cached(load_q)
+
+    def getq(e):
+        return getall(e)[0]
+
+    experts = _pick_experts(counts.cpu().numpy(), np.random.default_rng(0))
+    _check_whole_experts(cfg, x, ptok, offsets, y, experts, lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e)))
+    clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
+    tok = np.sort(np.random.default_rng(1).choice(clean, size=256, replace=False))
+    xn = np64(x)
+    # the oracle's FP8 layer and the layer with x and h unquantised, expert by expert
+    yq = np.zeros((tok.size, cfg.d))
+    yu = np.zeros((tok.size, cfg.d))
+    xs = xn[tok]
+    sel, g = ref["idx"][tok], ref["gate"][tok]
+    for e in list(range(cfg.E, cfg.E + cfg.S)) + [int(v) for v in np.unique(sel)]:
+        rows, slot = (np.arange(tok.size), None) if e >= cfg.E else np.nonzero(sel == e)
+        w = 1.0 if slot is None else g[rows, slot][:, None]
+        q, wgu_e, wd_e = getall(e)
+        yq[rows] += w * Q.fp8_swiglu_expert(xs[rows], *q)
+        yu[rows] += w * O.swiglu_expert(xs[rows], wgu_e, wd_e)
+    o = np64(out)[tok]
+    r = errs(o, yq)
+    _report("v3fp8 layer output vs the oracle's FP8 layer (256 tokens)", r)
+    ru = errs(o, yu)
+    _report("v3fp8 layer output vs the unquantised layer (256 tokens)", ru)
+    assert r["out_err"] < TOL_MAX and r["fro"] < TOL_FRO
+    assert ru["fro"] < TOL_FRO_FP8_UNQUANTISED

@@ -7,11 +7,18 @@ import torch
 from oracle import moe_oracle as O
 from sparse_moe_layer_12_b300 import binding as B
 from sparse_moe_layer_12_b300 import inputs as I
-from moe_testutil import check_routing, np64, oracle_route, out_err, rel_err
+from moe_testutil import check_routing, errs, np64, oracle_route, out_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 TOL_BF16 = 2e-2  # computation error / RMS(ref), on top of the bf16 storage rounding (see out_err)
+TOL_FRO = 5e-3  # relative Frobenius error: h, y and out rounded to bf16 once each (about 2e-3 together)
+
+
+def _assert_close(tag, got, want):
+    e = errs(got, want)
+    print(f"{tag}: out_err {e['out_err']:.3e}  max/RMS {e['max_rms']:.3e}  Frobenius {e['fro']:.3e}")
+    assert e["out_err"] < TOL_BF16 and e["fro"] < TOL_FRO, tag
 
 
 def _shape(cfg, fp8=False):
@@ -71,9 +78,9 @@ def test_expert_ffn_groups(libmoe, name):
     xn = np64(x)
     Tk = cfg.T * cfg.k
     yg = np64(y)
-    # every routed group up to 12 experts (all of them for small layers), shared experts on <= 512 tokens
+    # every routed group, shared experts on <= 512 tokens
     got, want = [], []
-    for e in range(min(cfg.E, 12)):
+    for e in range(cfg.E):
         lo, hi = p["offsets"][e], p["offsets"][e + 1]
         if hi > lo:
             want.append(O.swiglu_expert(xn[p["perm_token"][lo:hi]], np64(wgu[e]), np64(wd[e])))
@@ -82,10 +89,7 @@ def test_expert_ffn_groups(libmoe, name):
     for si in range(cfg.S):
         want.append(O.swiglu_expert(xn[:nt], np64(wgu[cfg.E + si]), np64(wd[cfg.E + si])))
         got.append(yg[Tk + si * cfg.T: Tk + si * cfg.T + nt])
-    got, want = np.concatenate(got), np.concatenate(want)
-    err = out_err(got, want)
-    print(f"{name}: expert FFN err {err:.3e} (plain max/RMS {rel_err(got, want):.3e})")
-    assert err < TOL_BF16
+    _assert_close(f"{name}: expert FFN, every expert", np.concatenate(got), np.concatenate(want))
 
 
 def test_combine(libmoe):
@@ -113,9 +117,8 @@ def test_forward_full(libmoe, name):
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     tok = clean[:: max(1, cfg.T // 256)]  # every token of tiny, 256 spread tokens of mid
     yr = O.forward_rows(tok, np64(x), ref, lambda e: (np64(wgu[e]), np64(wd[e])), cfg.E, cfg.S)
-    err = out_err(np64(out)[tok], yr)
-    print(f"{name}: forward err {err:.3e} (plain max/RMS {rel_err(np64(out)[tok], yr):.3e}), near-tied tokens {ties}")
-    assert err < TOL_BF16
+    print(f"{name}: near-tied tokens {ties}")
+    _assert_close(f"{name}: forward", np64(out)[tok], yr)
     out2, *_ = B.moe_forward(s, x, wr, b.clone(), wgu, wd, ws=ws)
     assert torch.equal(out, out2), "forward is deterministic"
     assert B.moe_get_device_status(ws) == 0
@@ -137,25 +140,11 @@ def _sampled_check(cfg, x, wr, b, wgu, wd, out, idx, gate, counts, logit_offset=
         return cache[e]
 
     yr = O.forward_rows(tok, np64(x), ref, get_expert, cfg.E, cfg.S)
-    err = out_err(np64(out)[tok], yr)
-    print(f"{cfg.name}: sampled err {err:.3e} (plain max/RMS {rel_err(np64(out)[tok], yr):.3e})")
-    return err, ties
-
-
-def test_forward_v3_sampled(libmoe):
-    cfg = I.CONFIGS["v3"]
-    x = I.make_x(cfg, DEV)
-    wr = I.make_router(cfg, DEV)
-    b = I.make_bias(cfg, DEV)
-    wgu, wd = I.make_experts(cfg, DEV)
-    s = _shape(cfg)
-    ws = B.alloc_workspace(s)
-    out, idx, gate, counts = B.moe_forward(s, x, wr, b.clone(), wgu, wd, ws=ws)
-    torch.cuda.synchronize()
-    err, ties = _sampled_check(cfg, x, wr, b, wgu, wd, out, idx, gate, counts)
-    print(f"v3: sampled max rel err {err:.3e}, near-tied tokens {ties}")
-    assert err < TOL_BF16
-    assert B.moe_get_device_status(ws) == 0
+    e = errs(np64(out)[tok], yr)
+    print(f"{cfg.name}: sampled out_err {e['out_err']:.3e} (plain max/RMS {e['max_rms']:.3e}, "
+          f"Frobenius {e['fro']:.3e})")
+    assert e["fro"] < TOL_FRO
+    return e["out_err"], ties
 
 
 def test_skew_bias_trajectory(libmoe):
@@ -215,7 +204,7 @@ def test_forward_group_limited(libmoe):
     check_routing(ref, idx, gate, counts, offsets, cfg.E, 4, 2)
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     yr = O.forward_rows(clean, np64(x), ref, lambda e: (np64(wgu[e]), np64(wd[e])), cfg.E, cfg.S)
-    assert out_err(np64(out)[clean], yr) < TOL_BF16
+    _assert_close("group-limited forward", np64(out)[clean], yr)
 
 
 def test_forward_no_tokens(libmoe):
