@@ -11,8 +11,12 @@ Frobenius error, which a dropped term or a wrong index cannot pass.
 
 bf16: out_err <= 2e-2, Frobenius <= 5e-3 (h, y and out are each rounded to bf16
 once: 2^-9 / sqrt(3) RMS relative error each, about 2e-3 together).
-FP8: against the oracle's FP8 layer (same 1x128 / 128x128 quantisation) the same
-bounds as bf16, since both sides quantise the same values; against the layer with
+FP8: against the oracle's FP8 layer (same 1x128 / 128x128 quantisation) Frobenius
+<= 5e-3 as bf16, since both sides quantise the same values, and out_err <= 3e-2:
+where h lies within the FP32-vs-float64 difference of a rounding midpoint the two
+sides pick neighbouring E4M3 codes, one step of 32/448 of the tile's amax, which
+reaches an output through a W_down element of up to ~4.5/sqrt(I), 2.8 % of the
+output RMS (measured: 1.8e-2 on one V3 expert); against the layer with
 x and h left unquantised the relative Frobenius error must stay below 6e-2 (E4M3's
 three mantissa bits alone cost about 4.4 %, and its max error, 20-30 % of the RMS,
 is reported only).
@@ -30,6 +34,7 @@ from moe_testutil import check_routing, errs, np64, oracle_route
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 TOL_MAX = 2e-2
+TOL_MAX_FP8 = 3e-2  # one E4M3 code flip of h (see above)
 TOL_FRO = 5e-3
 TOL_FRO_FP8_UNQUANTISED = 6e-2
 
@@ -75,7 +80,7 @@ def _report(tag, e):
     print(f"{tag}: out_err {e['out_err']:.3e}  max/RMS {e['max_rms']:.3e}  Frobenius {e['fro']:.3e}")
 
 
-def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, fro_tol=TOL_FRO):
+def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, max_tol=TOL_MAX):
     xn = np64(x)
     ptok = ptok.cpu().numpy()
     off = offsets.cpu().numpy()
@@ -86,7 +91,7 @@ def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, fro_tol=T
         got = np64(yg[lo:hi])
         r = errs(got, want)
         _report(f"{cfg.name} expert {e} ({hi - lo} tokens)", r)
-        assert r["out_err"] < TOL_MAX and r["fro"] < fro_tol, e
+        assert r["out_err"] < max_tol and r["fro"] < TOL_FRO, e
     Tk = cfg.T * cfg.k
     tok = _shared_rows(cfg.T)
     for si in range(cfg.S):
@@ -94,7 +99,7 @@ def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, fro_tol=T
         got = np64(yg[torch.as_tensor(Tk + si * cfg.T + tok, device=yg.device)])
         r = errs(got, want)
         _report(f"{cfg.name} shared expert {si} ({tok.size} tokens)", r)
-        assert r["out_err"] < TOL_MAX and r["fro"] < fro_tol
+        assert r["out_err"] < max_tol and r["fro"] < TOL_FRO
 
 
 def _cached(fn):
@@ -150,7 +155,8 @@ def test_v3_fp8_whole_experts_and_output(libmoe):
         return getall(e)[0]
 
     experts = _pick_experts(counts.cpu().numpy(), np.random.default_rng(0))
-    _check_whole_experts(cfg, x, ptok, offsets, y, experts, lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e)))
+    _check_whole_experts(cfg, x, ptok, offsets, y, experts, lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e)),
+                         max_tol=TOL_MAX_FP8)
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     tok = np.sort(np.random.default_rng(1).choice(clean, size=256, replace=False))
     xn = np64(x)
@@ -170,5 +176,5 @@ def test_v3_fp8_whole_experts_and_output(libmoe):
     _report("v3fp8 layer output vs the oracle's FP8 layer (256 tokens)", r)
     ru = errs(o, yu)
     _report("v3fp8 layer output vs the unquantised layer (256 tokens)", ru)
-    assert r["out_err"] < TOL_MAX and r["fro"] < TOL_FRO
+    assert r["out_err"] < TOL_MAX_FP8 and r["fro"] < TOL_FRO
     assert ru["fro"] < TOL_FRO_FP8_UNQUANTISED
