@@ -16,6 +16,14 @@ step, far more than the 126 MB L2.
 Prints one JSON line (rank 0).  Multi-GPU (torchrun, one rank per GPU): every
 rank runs its own T tokens (weak scaling) and the per-expert counts are summed
 across ranks before the bias update, so every replica keeps the same bias.
+
+The default one-GPU line (V3 bf16) also carries: `stages` (CUDA-event times of the
+router, permute and combine calls against their algorithmic bytes, and the expert
+FFN's per-step spread), `skew` (the skewed-load decode workload, T=256, 20 forward +
+bias-update steps with the per-step max/mean load), `fp8` (the V3-shaped FP8
+workload, T=16384, against the FP8 dense peak measured in the same run),
+`backward`, `cpu_baseline` and `routing_check` (the oracle's near-tied tokens and
+any untied token the GPU routed differently).
 """
 from __future__ import annotations
 
@@ -98,7 +106,7 @@ class Clocks:
     def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                       "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
 
@@ -122,11 +130,13 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_experts=6, n_tok=512):
+def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_experts=6, n_tok=512, gpu_idx=None):
     """Times the oracle on the host cores on a bounded sample of the workload and
     extrapolates to the whole step (tokens/s).  Router and permutation run on all T
     tokens; the expert FFN runs on a sample of routed experts (all their tokens)
-    plus the shared experts on n_tok tokens, scaled by FLOPs; combine on all tokens."""
+    plus the shared experts on n_tok tokens, scaled by FLOPs; combine on all tokens.
+    gpu_idx: the GPU router's choice for the same x, w_router and bias; the result then
+    carries a `routing_check` (near-tied tokens, untied tokens routed differently)."""
     import numpy as np
 
     from oracle import moe_oracle as O
@@ -171,7 +181,15 @@ def cpu_oracle_sample(cfg, x, w_router, bias, wgu, wd, logit_offset=None, n_expe
     t_comb = time.perf_counter() - t2
     t_total = t_route + t_comb + t_ffn * (cfg.expert_flops() / flops_done)
     cores = len(os.sched_getaffinity(0))
+    check = None
+    if gpu_idx is not None:
+        tied = r["boundary_tie"] | r["order_tie"]
+        check = {"tokens": int(cfg.T), "near_tied": int(tied.sum()),
+                 "untied_routed_differently": int(np.any(gpu_idx[~tied] != r["idx"][~tied], axis=1).sum()),
+                 "tied_with_another_choice": int(np.any(gpu_idx[tied] != r["idx"][tied], axis=1).sum()),
+                 "rule": "near-tied: biased scores within 1e-5 at the k-th place or inside the chosen set"}
     return {
+        "routing_check": check,
         "value": cfg.T / t_total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
         "sample": (f"{cfg.name}: router+permute+combine+bias update on all {cfg.T} tokens; expert FFN on "
                    f"{len(experts)} routed experts (all their tokens) + {cfg.S} shared on {n_tok} tokens, "
@@ -238,8 +256,27 @@ def _setup_dist():
     return world, rank, local
 
 
+def _config_obj(cfg, world):
+    """The `config` object both arms print (so the driver sees the same workload)."""
+    return {"workload": f"{cfg.name}: T={cfg.T}/GPU d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}",
+            "global_batch": world * cfg.T, "parallelism": f"dp{world} (token-sharded replicas)",
+            "l2": _l2_note(cfg)}
+
+
+def _cpu_sample(cfg) -> tuple[int, int]:
+    """The oracle's bounded sample (routed experts timed whole, shared-expert tokens), the
+    same in the reference arm and in the cpu_baseline leg; the FP8 oracle also simulates
+    the quantisation, so it samples less."""
+    return (2, 256) if cfg.fp8 else (6, 512)
+
+
 def run_reference(args):
-    """The oracle (CPU) on this arm's workload, each step a bounded sample."""
+    """The oracle (CPU) on this arm's workload.  Each timed step is one bounded sample
+    (router, permutation, combine and bias update on all T tokens, the expert FFN on a
+    few whole routed experts plus the shared experts on a few hundred tokens);
+    `value` extrapolates the sample to the whole step by FLOPs, `ms_per_step` is the
+    measured time of one sample, and `tokens_per_step` the tokens that time stands
+    for, so that value = tokens_per_step / ms_per_step."""
     import torch
 
     from sparse_moe_layer_12_b300 import inputs as I
@@ -256,20 +293,22 @@ def run_reference(args):
     off = I.make_logit_offset(cfg, dev)
     lazy = _LazyExperts(cfg, dev)
     wgu, wd = lazy.gu, lazy.dn
-    for _ in range(args.warmup if args.warmup < 1 else 1):
+    for _ in range(min(args.warmup, 1)):
         cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=1, n_tok=64)
     vals = []
     t0 = time.perf_counter()
+    n_exp, n_tok = _cpu_sample(cfg)
     for _ in range(args.steps):
-        vals.append(cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=2, n_tok=128))
+        vals.append(cpu_oracle_sample(cfg, x, wr, b, wgu, wd, off, n_experts=n_exp, n_tok=n_tok))
     wall = time.perf_counter() - t0
     v = statistics.median([c["value"] for c in vals])
+    sample_s = statistics.median([c["seconds_measured"] for c in vals])
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * sample_s,
+        "extrapolated": True, "tokens_per_step": v * sample_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{cfg.name} T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} k={cfg.k} "
-                                                    f"I={cfg.I}", "l2": _l2_note(cfg)},
+        "data": "synthetic", "config": _config_obj(cfg, world),
         "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v,
                          "unit": "tokens/s"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -362,6 +401,146 @@ def run_backward_only(args):
     print(json.dumps({"stage": "backward", "workload": cfg.name, **r}), flush=True)
 
 
+def _stage_bytes(cfg, gathers: bool) -> dict:
+    """Algorithmic bytes per call of the HBM-bound stages (one layer step)."""
+    T, d, E, S, k = cfg.T, cfg.d, cfg.E, cfg.S, cfg.k
+    es = 1 if cfg.fp8 else 2
+    route = T * d * 2 + E * d * 2 + T * k * 8 + 8 * E
+    if gathers:  # tables only: read idx, write perm_token and inv_pos
+        permute = T * k * 4 * 3
+    else:
+        permute = T * d * 2 + T * k * d * es + (T * k * (d // 128) * 4 if cfg.fp8 else 0)
+    combine = (T * k + S * T) * d * 2 + T * d * 2
+    return {"route": route, "permute": permute, "combine": combine}
+
+
+_STAGES = ("route", "permute", "expert_ffn", "combine", "bias_update")
+
+
+def _make_step(B, dp, cfg, shape, x, wr, bias, off, wgu, wd, wgu_s, wd_s, ws, world, gathers, stream):
+    """One layer step through the separate C-ABI calls (the dispatch form moe_forward
+    picks for the shape), with optional CUDA events between the stages."""
+    import torch
+
+    fp8 = cfg.fp8
+    act_dtype = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    dev = x.device
+    y_buf = torch.empty(cfg.rows_total, cfg.d, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    xp_buf = None if gathers else torch.empty(cfg.rows_routed, cfg.d, dtype=act_dtype, device=dev)
+    xps_buf = (torch.empty(cfg.rows_routed, cfg.d // 128, dtype=torch.float32, device=dev)
+               if fp8 and not gathers else None)
+
+    def gpu_update(c, b, T_global, gamma):  # bias update from the global load (every rank the same)
+        B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group,
+                                       cfg.topk_group), c, b, gamma)
+
+    state = {}
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        idx, gate, counts, offsets = B.moe_route(shape, x, wr, bias, off, ws=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        xp, xps, ptok, inv = B.moe_permute(shape, x, idx, offsets, ws=ws, rows=not gathers, x_perm=xp_buf,
+                                           x_perm_scale=xps_buf)
+        if ev is not None:
+            ev[2].record(stream)
+        if gathers:
+            y = B.moe_expert_ffn_gather(shape, x, ptok, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
+        else:
+            y = B.moe_expert_ffn(shape, xp, xps, x, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
+        if ev is not None:
+            ev[3].record(stream)
+        B.moe_combine(shape, y, gate, inv, out=out)
+        if ev is not None:
+            ev[4].record(stream)
+        dp.bias_update_global(counts, bias, cfg.T * world, cfg.gamma, gpu_update)
+        if ev is not None:
+            ev[5].record(stream)
+        state.update(idx=idx, counts=counts)
+
+    return step, out, state, gpu_update
+
+
+def _timed_steps(step, steps, warmup, stream, world):
+    """W untimed steps, then K steps between two events (barrier + synchronise on both
+    sides for N > 1); per-step stage events.  Returns (total ms, per-stage ms lists)."""
+    import torch
+    import torch.distributed as dist
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    stages = {name: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, name in enumerate(_STAGES)}
+    return t0.elapsed_time(t1), stages
+
+
+def _stage_report(cfg, stages, gathers, pk, pk_src) -> dict:
+    nbytes = _stage_bytes(cfg, gathers)
+    rep = {}
+    for name in ("route", "permute", "combine"):
+        ms = statistics.median(stages[name])
+        gbs = nbytes[name] / (ms / 1e3) / 1e9
+        rep[name] = {"us": 1000.0 * ms, "algorithmic_bytes": nbytes[name], "GB/s": gbs,
+                     "frac_of_hbm": gbs / pk["hbm_gbs"], "frac_of_8TBs_spec": gbs / 8000.0,
+                     "peak_source": f"{pk_src} HBM copy"}
+    rep["permute"]["form"] = "tables only (rows gathered in the GEMM)" if gathers else "permuted copy"
+    f = stages["expert_ffn"]
+    rep["expert_ffn"] = {"ms_mean": statistics.mean(f), "ms_min": min(f), "ms_median": statistics.median(f),
+                         "ms_max": max(f)}
+    rep["bias_update"] = {"us": 1000.0 * statistics.median(stages["bias_update"])}
+    return rep
+
+
+def _fp8_dense_peak(dev):
+    """Dense FP8 (E4M3 x E4M3 -> bf16) and bf16 GEMM throughput of this GPU at 8192^3,
+    best of 10 (torch._scaled_mm with unit scales, torch.matmul): the FP8 roofline."""
+    import torch
+
+    n = 8192
+    res = {}
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        ab, bb = torch.randn(n, n, device=dev, dtype=torch.bfloat16), torch.randn(n, n, device=dev,
+                                                                                  dtype=torch.bfloat16)
+        for name, fn in (("fp8", lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)),
+                         ("bf16", lambda: ab @ bb)):
+            for _ in range(3):
+                fn()
+            best = float("inf")
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            res[name] = 2.0 * n ** 3 / (best / 1e3) / 1e12
+        del a, b, ab, bb
+    except Exception as exc:  # no FP8 GEMM in this torch build: fall back to the nominal ratio
+        res["error"] = str(exc)[:200]
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -377,74 +556,32 @@ def run_ours(args):
     B.load()
     fp8 = cfg.fp8
     shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group)
-
-    def gpu_update(c, b, T_global, gamma):  # bias update from the global load (every rank the same)
-        B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group), c, b, gamma)
+    pk, pk_src = _peaks()
+    main_run = world == 1 and not args.set and cfg.name == "v3"  # the default line: add the other workloads
 
     x = I.make_x(cfg_r, dev)
     wr = I.make_router(cfg, dev)
     bias = I.make_bias(cfg, dev)
     off = I.make_logit_offset(cfg, dev)
-    wgu, wd = I.make_experts(cfg, dev)
     wgu_s = wd_s = None
     if fp8:
-        wgu_b, wd_b = wgu, wd
-        wgu, wgu_s = B.moe_quantize_weights_fp8(wgu_b)
-        wd, wd_s = B.moe_quantize_weights_fp8(wd_b)
-        del wgu_b, wd_b
+        wgu, wgu_s, wd, wd_s = I.make_experts_fp8(cfg, dev)
+    else:
+        wgu, wd = I.make_experts(cfg, dev)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     ws = B.alloc_workspace(shape, dev)
-    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-
-    y_buf = torch.empty(cfg.rows_total, cfg.d, dtype=torch.bfloat16, device=dev)
     gathers = B.forward_gathers(shape)
-    act_dtype = torch.float8_e4m3fn if fp8 else torch.bfloat16
-    xp_buf = None if gathers else torch.empty(cfg.rows_routed, cfg.d, dtype=act_dtype, device=dev)
-    xps_buf = (torch.empty(cfg.rows_routed, cfg.d // 128, dtype=torch.float32, device=dev)
-               if fp8 and not gathers else None)
+    step, out, state, gpu_update = _make_step(B, dp, cfg, shape, x, wr, bias, off, wgu, wd, wgu_s, wd_s, ws, world,
+                                              gathers, stream)
 
-    def step(ev=None):
-        # the layer as moe_forward runs it, through its separate calls so that the
-        # expert FFN can be timed on its own; the dispatch form is moe_forward's
-        idx, gate, counts, offsets = B.moe_route(shape, x, wr, bias, off, ws=ws)
-        xp, xps, ptok, inv = B.moe_permute(shape, x, idx, offsets, ws=ws, rows=not gathers, x_perm=xp_buf,
-                                           x_perm_scale=xps_buf)
-        if ev is not None:
-            ev[0].record(stream)
-        if gathers:
-            y = B.moe_expert_ffn_gather(shape, x, ptok, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
-        else:
-            y = B.moe_expert_ffn(shape, xp, xps, x, offsets, wgu, wd, wgu_s, wd_s, ws=ws, y=y_buf)
-        if ev is not None:
-            ev[1].record(stream)
-        B.moe_combine(shape, y, gate, inv, out=out)
-        dp.bias_update_global(counts, bias, cfg.T * world, cfg.gamma, gpu_update)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
     clocks = Clocks()
     clocks.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ms, stages = _timed_steps(step, args.steps, args.warmup, stream, world)
     ck = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    ffn_ms = [a.elapsed_time(b) for a, b in evs]
+    ffn_ms = stages["expert_ffn"]
     eager_ms = ms
 
     # ---- the same step replayed from a CUDA graph (one launch of the whole step's
@@ -488,7 +625,6 @@ def run_ours(args):
         outh = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         xd = [torch.empty_like(x) for _ in range(2)]
         outd = [torch.empty_like(out) for _ in range(2)]
-        counts_d = torch.empty(cfg.E, dtype=torch.int32, device=dev)
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("x_ready", "x_free", "out_ready", "out_free")}
         for k in ("x_free", "out_free"):
@@ -536,20 +672,23 @@ def run_ours(args):
                "ms_per_step": e_ms / args.steps,
                "how": "moe_forward through the C ABI; x from pinned host memory and out back to it every step, "
                       "copies on two side streams overlapping the neighbouring steps"}
-        del counts_d
 
     if rank != 0:
         if world > 1:
             dist.barrier()
             dist.destroy_process_group()
         return
-    pk, pk_src = _peaks()
+    fp8_peaks = _fp8_dense_peak(dev) if (fp8 or main_run) else {}
     flops = cfg.expert_flops()
     ffn_avg_s = statistics.mean(ffn_ms) / 1e3
     achieved = flops / ffn_avg_s / 1e12
-    peak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    if fp8 and "fp8" in fp8_peaks:
+        peak, peak_src = fp8_peaks["fp8"], "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
+    else:
+        peak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
+        peak_src = f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if fp8 else "")
     # weight bytes the expert GEMMs must stream: every expert that received a token, plus shared
-    _, _, c_last, _ = B.moe_route(shape, x, wr, bias, off, ws=ws)
+    c_last = state["counts"]
     hit = int((c_last > 0).sum().item()) + cfg.S
     wbytes = hit * 3.0 * cfg.d * cfg.I * (1.0 if fp8 else 2.0)
     ridge = peak * 1e12 / (pk["hbm_gbs"] * 1e9)
@@ -561,8 +700,8 @@ def run_ours(args):
     else:
         roofline = {"bound": "tensor", "kernel": "moe_expert_ffn (grouped gate/up+SwiGLU and down GEMMs)",
                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "peak_source": f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
-                    "algorithmic_flops": flops, "traffic": _traffic(fp8) if cfg.name in ("v3", "v3fp8") else None}
+                    "peak_source": peak_src, "algorithmic_flops": flops,
+                    "traffic": _traffic(fp8) if cfg.name in ("v3", "v3fp8") else None}
     line = {
         "metric": METRIC,
         "value": world * cfg.T * args.steps / (ms / 1e3),
@@ -576,12 +715,11 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "fp8-e4m3 (fp32 acc)" if fp8 else "bf16 (fp32 acc)",
         "data": "synthetic (seeded, random-init weights of the layer's shape)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T}/GPU d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}",
-                   "global_batch": world * cfg.T, "parallelism": f"dp{world} (token-sharded replicas)",
-                   "l2": _l2_note(cfg)},
+        "config": _config_obj(cfg, world),
         "expert_gemm_tflops": achieved,
         "expert_gemm_pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline,
+        "stages": _stage_report(cfg, stages, gathers, pk, pk_src),
         "stage_ms": {"expert_ffn": statistics.mean(ffn_ms), "rest": eager_ms / args.steps - statistics.mean(ffn_ms)},
         "timing": {"eager_ms_per_step": eager_ms / args.steps,
                    "graph_ms_per_step": None if graph_ms is None else graph_ms / args.steps,
@@ -593,30 +731,119 @@ def run_ours(args):
         "clocks": ck,
         "e2e": e2e,
     }
+    if fp8_peaks:
+        line["dense_peaks_this_run"] = {**{f"{k}_tflops": v for k, v in fp8_peaks.items() if k != "error"},
+                                        **({"error": fp8_peaks["error"]} if "error" in fp8_peaks else {}),
+                                        "how": "8192^3 GEMM, best of 10, CUDA events"}
     if cfg.zipf_amp and world == 1:
-        # the skewed decode workload: 20 forward + bias-update steps from b = 0, per-step max/mean load
-        b20 = torch.zeros_like(bias)
-        loads = []
-        for _ in range(20):
-            _, _, _, c = B.moe_forward(shape, x, wr, b20, wgu, wd, logit_offset=off, w_gu_scale=wgu_s,
-                                       w_down_scale=wd_s, gamma=cfg.gamma, update_bias=True, ws=ws, out=out)
-            cc = c.float()
-            loads.append(round(float(cc.max() / cc.mean()), 3))
-        line["load_max_over_mean_per_step"] = loads
-    if world == 1 and not fp8 and not args.no_backward:
+        line["skew"] = _skew_run(B, dp, cfg, x, wr, off, wgu, wd, wgu_s, wd_s, ws, stream, pk, pk_src)
+    # the router's choice for the workload's initial bias, for the oracle leg's routing check
+    b0 = I.make_bias(cfg, dev)
+    gpu_idx = B.moe_route(shape, x, wr, b0, off, ws=ws)[0].cpu().numpy()
+    del ws
+    torch.cuda.empty_cache()
+    if main_run and not args.no_backward:
         # the layer's backward pass on the same weights (a row beyond the forward's hot path;
         # not part of `value`)
         line["backward"] = _time_backward(cfg, x, wr, bias, off, wgu, wd, args.steps, args.warmup)
-    if world == 1 and not args.no_cpu_baseline:
-        del ws, wgu, wd
+    if main_run:
+        # the skewed decode workload (T=256, V3 widths, Zipf logit offsets): the same
+        # weights (same seeds), 20 forward + bias-update steps from b = 0
+        sk = I.CONFIGS["skew"]
+        sk_shape = B.make_shape(sk.T, sk.d, sk.E, sk.S, sk.k, sk.I)
+        sk_ws = B.alloc_workspace(sk_shape, dev)
+        line["skew"] = _skew_run(B, dp, sk, I.make_x(sk, dev), I.make_router(sk, dev), I.make_logit_offset(sk, dev),
+                                 wgu, wd, None, None, sk_ws, stream, pk, pk_src)
+        del sk_ws
+        del wgu, wd
         torch.cuda.empty_cache()
+        line["fp8"] = _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks)
+    if world == 1 and not args.no_cpu_baseline:
         wgu_c = _LazyExperts(cfg, dev)
-        line["cpu_baseline"] = cpu_oracle_sample(cfg, x, wr, bias, wgu_c.gu, wgu_c.dn, off,
-                                                 n_experts=2 if fp8 else 6)
+        n_exp, n_tok = _cpu_sample(cfg)
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, x, wr, b0, wgu_c.gu, wgu_c.dn, off, n_experts=n_exp,
+                                                 n_tok=n_tok, gpu_idx=gpu_idx)
+        rc = line["cpu_baseline"].pop("routing_check", None)
+        if rc is not None:
+            line["routing_check"] = rc
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def _skew_run(B, dp, cfg, x, wr, off, wgu, wd, wgu_s, wd_s, ws, stream, pk, pk_src, steps=20):
+    """The skewed-load decode regime: `steps` forward + bias-update steps from b = 0 on one
+    batch, each timed with CUDA events; per-step max/mean expert load; the expert FFN is
+    bound by streaming the weights of the experts that received tokens."""
+    import torch
+
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I)
+    gathers = B.forward_gathers(shape)
+    bias = torch.zeros(cfg.E, dtype=torch.float32, device=x.device)
+    step, _, state, _ = _make_step(B, dp, cfg, shape, x, wr, bias, off, wgu, wd, wgu_s, wd_s, ws, 1, gathers,
+                                   stream)
+    for _ in range(3):  # warm-up on a throw-away bias
+        step()
+    bias.zero_()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    loads, hits = [], []
+    for i in range(steps):
+        step(evs[i])
+        c = state["counts"].float()
+        loads.append(c)
+        hits.append((state["counts"] > 0).sum())
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    ffn_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    wbytes = [(int(h.item()) + cfg.S) * 3.0 * cfg.d * cfg.I * 2.0 for h in hits]
+    gbs = [b / (m / 1e3) / 1e9 for b, m in zip(wbytes, ffn_ms)]
+    return {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}, "
+                        f"Zipf(1.1) logit offsets A={cfg.zipf_amp}",
+            "steps": steps, "tokens_per_s": cfg.T * steps / (sum(step_ms) / 1e3),
+            "ms_per_step_median": statistics.median(step_ms),
+            "dispatch": "rows gathered from x inside the gate/up GEMM" if gathers else "permuted copy",
+            "load_max_over_mean_per_step": [round(float(c.max() / c.mean()), 3) for c in loads],
+            "experts_hit_per_step": [int(h.item()) for h in hits],
+            "expert_ffn_weight_stream": {"GB/s_median": statistics.median(gbs), "peak": pk["hbm_gbs"],
+                                         "frac_median": statistics.median(gbs) / pk["hbm_gbs"],
+                                         "peak_source": f"{pk_src} HBM copy",
+                                         "bytes": "bf16 weights of every expert that received a token, + shared"}}
+
+
+def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks):
+    """The V3-shaped FP8 workload (T=16384, E4M3 1x128 / 128x128, FP32 accumulation)."""
+    import torch
+
+    cfg = I.CONFIGS["v3fp8"]
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, True)
+    x, wr, bias = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
+    wgu, gs, wd, ds = I.make_experts_fp8(cfg, dev)
+    ws = B.alloc_workspace(shape, dev)
+    gathers = B.forward_gathers(shape)
+    step, _, _, _ = _make_step(B, dp, cfg, shape, x, wr, bias, None, wgu, wd, gs, ds, ws, 1, gathers, stream)
+    clocks = Clocks()
+    clocks.start()
+    time.sleep(0.3)
+    ms, stages = _timed_steps(step, args.steps, args.warmup, stream, 1)
+    ck = clocks.stop()
+    status = B.moe_get_device_status(ws)
+    ffn_s = statistics.mean(stages["expert_ffn"]) / 1e3
+    tf = cfg.expert_flops() / ffn_s / 1e12
+    if "fp8" in fp8_peaks:
+        peak, src = fp8_peaks["fp8"], "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
+    else:
+        peak, src = 2.0 * pk["bf16_tflops"], f"{pk_src} bf16 burst x2 (fp8 nominal ratio)"
+    res = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}, E4M3 "
+                       "1x128 activation tiles, 128x128 weight blocks, FP32 accumulation",
+           "tokens_per_s": cfg.T * args.steps / (ms / 1e3), "ms_per_step": ms / args.steps,
+           "steps": args.steps, "warmup": args.warmup,
+           "expert_gemm_tflops": tf, "fp8_peak_tflops": peak, "frac": tf / peak, "peak_source": src,
+           "stages": _stage_report(cfg, stages, gathers, pk, pk_src), "clocks": ck, "device_status": status}
+    del ws, wgu, wd, gs, ds, x
+    torch.cuda.empty_cache()
+    return res
 
 
 def main():
