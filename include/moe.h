@@ -283,6 +283,32 @@ MOE_API moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const
                                   void* dw_gate_up, void* dw_down, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* Expert parallelism ("DeepSeek-V3 Overview and Key Innovations", Training
+ * Infrastructure and Optimization: experts spread over GPUs, all-to-all dispatch
+ * and combine; "拆解DeepSeek V3": 8 GPUs per node over NVLink/NVSwitch).  The E
+ * routed experts are split into G contiguous ranges of E_loc = E / G, one per
+ * rank, so moe_permute's expert-major copy is already ordered by destination rank
+ * and the dispatch is one all-to-all of row ranges (done by the caller, e.g. with
+ * NCCL).  A rank then holds rows in source-major order: for each source rank s,
+ * the rows s sent for each local expert e in turn (tokens ascending).  This call
+ * moves rows between that order and the local expert-major order (expert e: the
+ * rows of every source s in turn) that moe_expert_ffn takes, and back:
+ *   recv_counts   int32 [G, E_loc]  rows source s sent for local expert e (device)
+ *   rows          the total of recv_counts (rows of src and dst)
+ *   src, dst      [rows, row_bytes] (row_bytes % 16 == 0; bf16 or E4M3 rows)
+ *   src_scale, dst_scale  f32 [rows, scale_cols] moved with the rows (FP8 1x128
+ *                 scales), or NULL with scale_cols = 0
+ *   local_offsets int32 [E_loc + 1] out or NULL: expert-major group offsets
+ *   to_local      1: source-major src -> expert-major dst (after the dispatch);
+ *                 0: expert-major src -> source-major dst (before the combine)
+ *   ws            a workspace as above (its status word only)
+ * Counts that are negative or do not add up to `rows` set MOE_ERR_DEVICE, move
+ * nothing and set local_offsets to zero.  Limits: G * E_loc <= 256. */
+MOE_API moe_status_t moe_ep_regroup(int G, int E_loc, const int32_t* recv_counts, int rows, const void* src,
+                                    void* dst, size_t row_bytes, const float* src_scale, float* dst_scale,
+                                    int scale_cols, int32_t* local_offsets, int to_local, void* ws,
+                                    moe_stream_t stream);
+
 /* Reads (synchronising `stream`) and clears the device status word in `ws`:
  * MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the read
  * itself fails).  `ws` must be a workspace used by the calls above. */

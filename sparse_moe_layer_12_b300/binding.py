@@ -24,7 +24,7 @@ EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", 
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
            "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static",
            "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward",
-           "moe_get_static_device_status"]
+           "moe_get_static_device_status", "moe_ep_regroup"]
 
 
 class MoEError(RuntimeError):
@@ -60,6 +60,7 @@ _SIGS = {
     "moe_backward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_device_status": (_I, [_P, _P]),
     "moe_get_static_device_status": (_I, [_P]),
+    "moe_ep_regroup": (_I, [_I, _I, _P, _I, _P, _P, _SZ, _P, _P, _I, _P, _I, _P, _P]),
     "moe_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_version": (ctypes.c_char_p, []),
@@ -359,6 +360,39 @@ def moe_backward(shape: Shape, x, w_router, w_gate_up, w_down, topk_idx, dout, l
         ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(w_gate_up), _ptr(w_down),
         _ptr(topk_idx), _ptr(dout), _ptr(dx), _ptr(dwr), _ptr(dwgu), _ptr(dwd), _ptr(ws), ws.numel(), _stream()))
     return dx, dwr, dwgu, dwd
+
+
+def moe_ep_regroup(recv_counts, src, to_local: bool, ws, src_scale=None, dst=None, dst_scale=None,
+                   local_offsets=None):
+    """Rows between source-major order (as received from the dispatch all-to-all) and
+    local expert-major order.  recv_counts int32 [G, E_loc] (CUDA); src [rows, ...]
+    (bf16 / E4M3 rows, row bytes a multiple of 16); src_scale f32 [rows, cols] or None.
+    Returns (dst, dst_scale, local_offsets int32 [E_loc + 1])."""
+    if not (recv_counts.is_cuda and recv_counts.dtype == torch.int32 and recv_counts.dim() == 2
+            and recv_counts.is_contiguous()):
+        raise ValueError("recv_counts must be a contiguous CUDA int32 tensor [G, E_loc]")
+    G, E_loc = recv_counts.shape
+    if not (src.is_cuda and src.is_contiguous() and src.dim() == 2):
+        raise ValueError("src must be a contiguous CUDA tensor [rows, cols]")
+    rows = src.shape[0]
+    row_bytes = src.shape[1] * src.element_size()
+    dst = torch.empty_like(src) if dst is None else dst
+    _need(dst, src.dtype, tuple(src.shape), "dst")
+    cols = 0
+    if src_scale is not None:
+        cols = src_scale.shape[1]
+        _need(src_scale, torch.float32, (rows, cols), "src_scale")
+        dst_scale = torch.empty_like(src_scale) if dst_scale is None else dst_scale
+        _need(dst_scale, torch.float32, (rows, cols), "dst_scale")
+    else:
+        dst_scale = None
+    if local_offsets is None:
+        local_offsets = torch.empty(E_loc + 1, dtype=torch.int32, device=src.device)
+    _need(local_offsets, torch.int32, (E_loc + 1,), "local_offsets")
+    _check("moe_ep_regroup", load().moe_ep_regroup(
+        G, E_loc, _ptr(recv_counts), rows, _ptr(src), _ptr(dst), row_bytes, _ptr(src_scale), _ptr(dst_scale), cols,
+        _ptr(local_offsets), 1 if to_local else 0, _ptr(ws), _stream()))
+    return dst, dst_scale, local_offsets
 
 
 def moe_get_device_status(ws) -> int:

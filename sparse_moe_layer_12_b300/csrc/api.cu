@@ -444,6 +444,22 @@ moe_status_t moe_backward(const moe_shape_t* shape, const void* x, const void* w
                          dw_down, ws, (cudaStream_t)stream);
 }
 
+moe_status_t moe_ep_regroup(int G, int E_loc, const int32_t* recv_counts, int rows, const void* src, void* dst,
+                            size_t row_bytes, const float* src_scale, float* dst_scale, int scale_cols,
+                            int32_t* local_offsets, int to_local, void* ws, moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_ep_regroup");
+  if (G < 1 || E_loc < 1 || (long long)G * E_loc > kMaxE || rows < 0 || scale_cols < 0) return MOE_ERR_INVALID_ARG;
+  if (row_bytes == 0 || row_bytes % 16 || row_bytes > (1u << 20)) return MOE_ERR_INVALID_ARG;
+  if (!recv_counts || ((!src || !dst) && rows > 0)) return MOE_ERR_INVALID_ARG;
+  if (scale_cols > 0 && rows > 0 && (!src_scale || !dst_scale)) return MOE_ERR_INVALID_ARG;
+  if ((long long)rows * (long long)(row_bytes / 16) >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_ALIGNMENT;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGNMENT;
+  return launch_ep_regroup(G, E_loc, recv_counts, rows, src, dst, row_bytes, src_scale, dst_scale, scale_cols,
+                           local_offsets, to_local ? 1 : 0, ws, (cudaStream_t)stream);
+}
+
 moe_status_t moe_get_device_status(void* ws, moe_stream_t stream) {
   if (!ws) return MOE_ERR_WORKSPACE;
   int h[2] = {0, 0};

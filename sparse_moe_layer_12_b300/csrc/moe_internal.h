@@ -32,6 +32,7 @@ enum Site : int {
   kSitePermute = 21,
   kSiteSchedule = 22,
   kSiteBackward = 31,
+  kSiteEp = 41,
   kSiteDebug = 90,
 };
 
@@ -152,5 +153,9 @@ moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, flo
 moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale,
                                   cudaStream_t st);
 moe_status_t launch_debug_wait(void* ws, unsigned limit_us, cudaStream_t st);
+// expert parallelism: rows between source-major and local expert-major order (csrc/ep.cu)
+moe_status_t launch_ep_regroup(int G, int E_loc, const int32_t* counts, int rows, const void* src, void* dst,
+                               size_t row_bytes, const float* src_scale, float* dst_scale, int scale_n,
+                               int32_t* local_offsets, int to_local, void* ws, cudaStream_t st);
 
 }  // namespace moe
