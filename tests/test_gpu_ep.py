@@ -2,7 +2,9 @@
 (a stable sort of the received rows by local expert), bit for bit, and the whole
 expert-parallel layer with G ranks emulated as threads of this process on one GPU
 (exchanges as device copies, no kernel waiting on another) against moe_forward on
-each rank's tokens and against the oracle."""
+each rank's tokens -- bit for bit: every output element of the expert GEMMs is summed
+over K in an order fixed by its feature block alone, whichever tokens share its tile --
+and against the oracle."""
 import threading
 
 import numpy as np
@@ -135,7 +137,7 @@ def test_ep_layer_matches_forward(libmoe, name, G, T):
         e = errs(np64(out), np64(ref_out))
         print(f"{name} EP rank {r}/{G}: vs moe_forward bit-identical {torch.equal(out, ref_out)}, "
               f"out_err {e['out_err']:.2e} Frobenius {e['fro']:.2e}")
-        assert e["fro"] < 1e-3
+        assert torch.equal(out, ref_out)
         counts_all += counts
         # against the oracle on 64 of the rank's tokens
         ref = oracle_route(xs[r], wr, bias, cfg.k)
@@ -163,4 +165,4 @@ def test_ep_layer_fp8(libmoe):
         e = errs(np64(out), np64(ref_out))
         print(f"tiny fp8 EP rank {r}/{G}: vs moe_forward bit-identical {torch.equal(out, ref_out)}, "
               f"out_err {e['out_err']:.2e} Frobenius {e['fro']:.2e}")
-        assert e["fro"] < 1e-3
+        assert torch.equal(out, ref_out)
