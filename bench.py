@@ -52,6 +52,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    p.add_argument("--no-extras", action="store_true",
+                   help="the V3 line without its skew and fp8 objects (profiling captures of the V3 step alone)")
     p.add_argument("--set", default="", help="override workload fields, e.g. T=512,E=16 (profiling slices)")
     p.add_argument("--only", default="", choices=["", "route", "backward"],
                    help="time one stage alone: the router, or the layer's backward pass")
@@ -557,7 +559,8 @@ def run_ours(args):
     fp8 = cfg.fp8
     shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group)
     pk, pk_src = _peaks()
-    main_run = world == 1 and not args.set and cfg.name == "v3"  # the default line: add the other workloads
+    # the default line: add the other workloads
+    main_run = world == 1 and not args.set and cfg.name == "v3" and not args.no_extras
 
     x = I.make_x(cfg_r, dev)
     wr = I.make_router(cfg, dev)
