@@ -435,7 +435,7 @@ def _make_step(B, dp, cfg, shape, x, wr, bias, off, wgu, wd, wgu_s, wd_s, ws, wo
 
     def gpu_update(c, b, T_global, gamma):  # bias update from the global load (every rank the same)
         B.moe_bias_update(B.make_shape(T_global, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group,
-                                       cfg.topk_group), c, b, gamma)
+                                       cfg.topk_group, cfg.pow2), c, b, gamma)
 
     state = {}
 
@@ -557,7 +557,7 @@ def run_ours(args):
     cfg_r = cfg.with_(seed=cfg.seed + rank)  # each rank its own tokens (weak scaling); same weights
     B.load()
     fp8 = cfg.fp8
-    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group)
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, cfg.n_group, cfg.topk_group, cfg.pow2)
     pk, pk_src = _peaks()
     # the default line: add the other workloads
     main_run = world == 1 and not args.set and cfg.name == "v3" and not args.no_extras
@@ -568,7 +568,7 @@ def run_ours(args):
     off = I.make_logit_offset(cfg, dev)
     wgu_s = wd_s = None
     if fp8:
-        wgu, wgu_s, wd, wd_s = I.make_experts_fp8(cfg, dev)
+        wgu, wgu_s, wd, wd_s = I.make_experts_fp8(cfg, dev, pow2=cfg.pow2)
     else:
         wgu, wd = I.make_experts(cfg, dev)
     torch.cuda.synchronize()
@@ -716,7 +716,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8-e4m3 (fp32 acc)" if fp8 else "bf16 (fp32 acc)",
+        "dtype": ("fp8-e4m3, power-of-two block scales (fp32 acc)" if cfg.pow2 else "fp8-e4m3 (fp32 acc)")
+        if fp8 else "bf16 (fp32 acc)",
         "data": "synthetic (seeded, random-init weights of the layer's shape)",
         "config": _config_obj(cfg, world),
         "expert_gemm_tflops": achieved,
@@ -760,7 +761,8 @@ def run_ours(args):
         del sk_ws
         del wgu, wd
         torch.cuda.empty_cache()
-        line["fp8"] = _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks)
+        line["fp8"] = _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks, "v3fp8")
+        line["fp8_pow2"] = _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks, "v3fp8p2")
     if world == 1 and not args.no_cpu_baseline:
         wgu_c = _LazyExperts(cfg, dev)
         n_exp, n_tok = _cpu_sample(cfg)
@@ -815,14 +817,15 @@ def _skew_run(B, dp, cfg, x, wr, off, wgu, wd, wgu_s, wd_s, ws, stream, pk, pk_s
                                          "bytes": "bf16 weights of every expert that received a token, + shared"}}
 
 
-def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks):
-    """The V3-shaped FP8 workload (T=16384, E4M3 1x128 / 128x128, FP32 accumulation)."""
+def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks, name):
+    """A V3-shaped FP8 workload (T=16384, E4M3 1x128 / 128x128, FP32 accumulation): v3fp8 with
+    FP32 scales, v3fp8p2 with power-of-two scales applied by the block-scaled MMA."""
     import torch
 
-    cfg = I.CONFIGS["v3fp8"]
-    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, True)
+    cfg = I.CONFIGS[name]
+    shape = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, True, pow2=cfg.pow2)
     x, wr, bias = I.make_x(cfg, dev), I.make_router(cfg, dev), I.make_bias(cfg, dev)
-    wgu, gs, wd, ds = I.make_experts_fp8(cfg, dev)
+    wgu, gs, wd, ds = I.make_experts_fp8(cfg, dev, pow2=cfg.pow2)
     ws = B.alloc_workspace(shape, dev)
     gathers = B.forward_gathers(shape)
     step, _, _, _ = _make_step(B, dp, cfg, shape, x, wr, bias, None, wgu, wd, gs, ds, ws, 1, gathers, stream)
@@ -839,7 +842,8 @@ def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks):
     else:
         peak, src = 2.0 * pk["bf16_tflops"], f"{pk_src} bf16 burst x2 (fp8 nominal ratio)"
     res = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}, E4M3 "
-                       "1x128 activation tiles, 128x128 weight blocks, FP32 accumulation",
+                       "1x128 activation tiles, 128x128 weight blocks, FP32 accumulation, "
+                       + ("power-of-two scales (block-scaled MMA)" if cfg.pow2 else "FP32 scales"),
            "tokens_per_s": cfg.T * args.steps / (ms / 1e3), "ms_per_step": ms / args.steps,
            "steps": args.steps, "warmup": args.warmup,
            "expert_gemm_tflops": tf, "fp8_peak_tflops": peak, "frac": tf / peak, "peak_source": src,

@@ -66,7 +66,17 @@ typedef enum {
   MOE_ERR_DEVICE = 7       /* device: an index or count was inconsistent  */
 } moe_status_t;
 
-typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_dtype_t;
+/* Arithmetic of the expert GEMMs.  FP8 ("DeepSeek-V3 详解" 4.2-4.3): E4M3 codes with one
+ * scale per 1x128 activation tile (per token per 128 channels) and per 128x128 weight
+ * block, FP32 accumulation, bf16 output.  The pages fix the granularity, not the scale
+ * format: MOE_FP8_E4M3 takes scale = amax / 448 in FP32 and promotes each 128-wide K
+ * block's partial product through registers; MOE_FP8_E4M3_POW2 takes the smallest power
+ * of two with amax <= 448 * scale (codes in (224, 448] at the tile maximum), which the
+ * tensor core applies itself as UE8M0 block scales (kind::mxf8f6f4), accumulating in FP32
+ * in TMEM.  Both keep the scales as FP32 arrays of the same shapes; POW2 scales must be
+ * powers of two (moe_permute and moe_quantize_weights_fp8_pow2 make them so).  POW2
+ * layers use the permuted copy (moe_expert_ffn_gather returns MOE_ERR_UNSUPPORTED). */
+typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1, MOE_FP8_E4M3_POW2 = 2 } moe_dtype_t;
 
 /* T tokens, d model width, E routed experts, S shared experts, k experts
  * chosen per token, I expert intermediate size; dtype of the expert GEMMs.
@@ -123,8 +133,8 @@ MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const vo
  *   x_perm_scale f32 [T*k, d/128] out FP8 only (1x128 tile scales), else NULL
  *   perm_token   int32 [T*k]   out    token of each permuted row
  *   inv_pos      int32 [T, k]  out    permuted row of (t, j)
- * FP8 quantisation (scale = amax/448 per 1x128 tile, RNE, saturating) is
- * done on the way.  Inconsistent idx/offsets set MOE_ERR_DEVICE.
+ * FP8 quantisation (per 1x128 tile, the scale of the layer's dtype, RNE,
+ * saturating) is done on the way.  Inconsistent idx/offsets set MOE_ERR_DEVICE.
  * x_perm = NULL (and x_perm_scale = NULL): only perm_token and inv_pos are
  * built, no row is copied -- the input of moe_expert_ffn_gather. */
 MOE_API moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t* topk_idx,
@@ -254,6 +264,12 @@ MOE_API moe_status_t moe_get_static_device_status(moe_stream_t stream);
  * 1 for an all-zero block).  Used once, before the FP8 layer runs. */
 MOE_API moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* w_q,
                                       float* w_scale, moe_stream_t stream);
+
+/* As moe_quantize_weights_fp8, with power-of-two block scales (the smallest power of
+ * two with amax <= 448 * scale, 1 for an all-zero block): the weights of a
+ * MOE_FP8_E4M3_POW2 layer. */
+MOE_API moe_status_t moe_quantize_weights_fp8_pow2(int G, int N, int K, const void* w, void* w_q,
+                                                   float* w_scale, moe_stream_t stream);
 
 /* Backward pass of the layer for the routing the forward chose (the gradients
  * that training needs; "DeepSeek-V3 详解" 2.2-2.3 for the layer, and

@@ -15,7 +15,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
-MOE_BF16, MOE_FP8_E4M3 = 0, 1
+MOE_BF16, MOE_FP8_E4M3, MOE_FP8_E4M3_POW2 = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 
@@ -24,7 +24,7 @@ EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_permute", "moe_expert_ffn", 
            "moe_bias_update", "moe_forward", "moe_quantize_weights_fp8", "moe_get_device_status",
            "moe_debug_wait_timeout", "moe_status_string", "moe_version", "moe_expert_ffn_static",
            "moe_expert_ffn_gather", "moe_forward_gathers", "moe_backward_workspace_bytes", "moe_backward",
-           "moe_get_static_device_status", "moe_ep_regroup"]
+           "moe_get_static_device_status", "moe_ep_regroup", "moe_quantize_weights_fp8_pow2"]
 
 
 class MoEError(RuntimeError):
@@ -55,6 +55,7 @@ _SIGS = {
     "moe_forward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P,
                          _SZ, _P]),
     "moe_quantize_weights_fp8": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "moe_quantize_weights_fp8_pow2": (_I, [_I, _I, _I, _P, _P, _P, _P]),
     "moe_forward_gathers": (_I, [ctypes.POINTER(Shape)]),
     "moe_backward_workspace_bytes": (_SZ, [ctypes.POINTER(Shape)]),
     "moe_backward": (_I, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -108,8 +109,15 @@ def _need(t: torch.Tensor, dtype, shape, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def make_shape(T, d, E, S, k, I, fp8=False, n_group=0, topk_group=0) -> Shape:
-    return Shape(T, d, E, S, k, I, MOE_FP8_E4M3 if fp8 else MOE_BF16, n_group, topk_group)
+def make_shape(T, d, E, S, k, I, fp8=False, n_group=0, topk_group=0, pow2=False) -> Shape:
+    """fp8: E4M3 expert GEMMs with FP32 1x128 / 128x128 scales; with pow2 as well, power-of-two
+    scales applied by the block-scaled tensor-core MMA."""
+    dtype = (MOE_FP8_E4M3_POW2 if pow2 else MOE_FP8_E4M3) if fp8 else MOE_BF16
+    return Shape(T, d, E, S, k, I, dtype, n_group, topk_group)
+
+
+def is_fp8(shape: Shape) -> bool:
+    return shape.dtype in (MOE_FP8_E4M3, MOE_FP8_E4M3_POW2)
 
 
 def forward_gathers(shape: Shape) -> bool:
@@ -134,7 +142,7 @@ def alloc_workspace(shape: Shape, device="cuda") -> torch.Tensor:
 
 
 def _act_dtype(shape: Shape):
-    return torch.float8_e4m3fn if shape.dtype == MOE_FP8_E4M3 else torch.bfloat16
+    return torch.float8_e4m3fn if is_fp8(shape) else torch.bfloat16
 
 
 def moe_route(shape: Shape, x, w_router, bias, logit_offset=None, ws=None):
@@ -159,7 +167,7 @@ def moe_permute(shape: Shape, x, topk_idx, offsets, ws=None, rows=True, x_perm=N
     """rows=False: only the permutation tables (x_perm and its scales are None).
     x_perm / x_perm_scale: optional preallocated outputs."""
     T, d, E, k = shape.T, shape.d, shape.E, shape.k
-    fp8 = shape.dtype == MOE_FP8_E4M3
+    fp8 = is_fp8(shape)
     _need(x, torch.bfloat16, (T, d), "x")
     _need(topk_idx, torch.int32, (T, k), "topk_idx")
     _need(offsets, torch.int32, (E + 1,), "offsets")
@@ -194,7 +202,7 @@ def moe_expert_ffn(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate_up, w_
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
     _need(w_down, wdt, (E + S, d, I), "w_down")
-    if shape.dtype == MOE_FP8_E4M3:
+    if is_fp8(shape):
         _need(x_perm_scale, torch.float32, (T * k, d // 128), "x_perm_scale")
         _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
         _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
@@ -219,7 +227,7 @@ def moe_expert_ffn_gather(shape: Shape, x, perm_token, offsets, w_gate_up, w_dow
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
     _need(w_down, wdt, (E + S, d, I), "w_down")
-    if shape.dtype == MOE_FP8_E4M3:
+    if is_fp8(shape):
         _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
         _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
     ws = alloc_workspace(shape, x.device) if ws is None else ws
@@ -244,7 +252,7 @@ def moe_expert_ffn_static(shape: Shape, x_perm, x_perm_scale, x, offsets, w_gate
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(w_gate_up, wdt, (E + S, 2 * I, d), "w_gate_up")
     _need(w_down, wdt, (E + S, d, I), "w_down")
-    if shape.dtype == MOE_FP8_E4M3:
+    if is_fp8(shape):
         _need(x_perm_scale, torch.float32, (T * k, d // 128), "x_perm_scale")
         _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
         _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
@@ -289,7 +297,7 @@ def moe_forward(shape: Shape, x, w_router, bias, w_gate_up, w_down, logit_offset
     _need(w_down, wdt, (E + S, d, I), "w_down")
     if logit_offset is not None:
         _need(logit_offset, torch.float32, (E,), "logit_offset")
-    if shape.dtype == MOE_FP8_E4M3:
+    if is_fp8(shape):
         _need(w_gu_scale, torch.float32, (E + S, 2 * I // 128, d // 128), "w_gu_scale")
         _need(w_down_scale, torch.float32, (E + S, d // 128, I // 128), "w_down_scale")
     ws = alloc_workspace(shape, x.device) if ws is None else ws
@@ -306,15 +314,15 @@ def moe_forward(shape: Shape, x, w_router, bias, w_gate_up, w_down, logit_offset
     return out, idx, gate, counts
 
 
-def moe_quantize_weights_fp8(w):
-    """bf16 [G, N, K] -> (E4M3 [G, N, K], f32 scales [G, N/128, K/128])."""
+def moe_quantize_weights_fp8(w, pow2=False):
+    """bf16 [G, N, K] -> (E4M3 [G, N, K], f32 scales [G, N/128, K/128]); pow2: power-of-two scales."""
     if not (w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 3 and w.is_contiguous()):
         raise ValueError("w must be a contiguous CUDA bf16 tensor [G, N, K]")
     G, N, K = w.shape
     wq = torch.empty(G, N, K, dtype=torch.float8_e4m3fn, device=w.device)
     sc = torch.empty(G, N // 128, K // 128, dtype=torch.float32, device=w.device)
-    _check("moe_quantize_weights_fp8", load().moe_quantize_weights_fp8(G, N, K, _ptr(w), _ptr(wq), _ptr(sc),
-                                                                       _stream()))
+    name = "moe_quantize_weights_fp8_pow2" if pow2 else "moe_quantize_weights_fp8"
+    _check(name, getattr(load(), name)(G, N, K, _ptr(w), _ptr(wq), _ptr(sc), _stream()))
     return wq, sc
 
 

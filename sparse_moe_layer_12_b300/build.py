@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = ["api.cu", "route.cu", "permute.cu", "expert_gemm.cu", "expert_gemm_fp8.cu", "combine.cu", "expert_ffn_static.cu",
-           "backward.cu", "ep.cu"]
+           "backward.cu", "ep.cu", "expert_gemm_mx.cu"]
 HEADERS = ["moe_device.cuh", "moe_internal.h"]
 LIB = os.path.join(PKG, "libmoe.so")
 STAMP = LIB + ".hash"

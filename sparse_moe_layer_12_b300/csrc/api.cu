@@ -20,7 +20,7 @@ bool shape_valid(const moe_shape_t* s) {
   if (s->T < 0 || s->d < 128 || s->I < 128 || s->E < 1 || s->S < 0 || s->k < 1) return false;
   if (s->d % 128 || s->I % 128 || s->d > 65536 || s->I > 65536) return false;
   if (s->k > s->E) return false;
-  if (s->dtype != MOE_BF16 && s->dtype != MOE_FP8_E4M3) return false;
+  if (s->dtype != MOE_BF16 && !is_fp8(s->dtype)) return false;
   if (s->n_group == 0) return s->topk_group == 0;
   if (s->n_group < 1 || s->n_group > 32 || s->E % s->n_group) return false;
   if (s->topk_group < 1 || s->topk_group > s->n_group) return false;
@@ -43,14 +43,17 @@ static bool shape_supported(const moe_shape_t& s) {
 // loads of a contiguous copy; measured on B300 it wins only while the batch is
 // small (T*k = 512: 0.030 ms against 0.053 ms; T*k = 2048: even; T*k = 24576:
 // 0.67 ms against 0.52 ms; T*k = 65536: 8.6 ms against 6.1 ms).
-bool forward_gathers(const moe_shape_t& s) { return (size_t)s.T * s.k <= kForwardGatherMaxRows; }
+bool forward_gathers(const moe_shape_t& s) {
+  // the block-scaled FP8 GEMM reads whole-tile boxes only
+  return s.dtype != MOE_FP8_E4M3_POW2 && (size_t)s.T * s.k <= kForwardGatherMaxRows;
+}
 
 WsLayout ws_layout(const moe_shape_t& s) {
   WsLayout L{};
   const size_t A = 1024;
   const size_t Tk = (size_t)s.T * s.k;
   const size_t rows = Tk + (size_t)s.S * s.T;
-  const bool f8 = s.dtype == MOE_FP8_E4M3;
+  const bool f8 = is_fp8(s.dtype);
   const size_t es = f8 ? 1 : 2;
   size_t o = 0;
   L.status = o;      o = align_up(o + 256, A);
@@ -77,7 +80,7 @@ WsLayout ffn_ws_layout(const moe_shape_t& s) {
   WsLayout L{};
   const size_t A = 1024;
   const size_t rows = (size_t)s.T * s.k + (size_t)s.S * s.T;
-  const bool f8 = s.dtype == MOE_FP8_E4M3;
+  const bool f8 = is_fp8(s.dtype);
   size_t o = 0;
   L.status = o;      o = align_up(o + 256, A);
   L.sched = o;       o = align_up(o + Schedule::bytes(s.E + s.S), A);
@@ -292,7 +295,7 @@ moe_status_t moe_permute(const moe_shape_t* shape, const void* x, const int32_t*
   if (!tok(x, s) || !tok(topk_idx, s) || !offsets || !tok(perm_token, s) || !tok(inv_pos, s))
     return MOE_ERR_INVALID_ARG;
   if (!x_perm && x_perm_scale) return MOE_ERR_INVALID_ARG;  // tables only: no rows, no scales
-  if (x_perm && s.dtype == MOE_FP8_E4M3 && !x_perm_scale) return MOE_ERR_INVALID_ARG;
+  if (x_perm && is_fp8(s.dtype) && !x_perm_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
   return launch_permute(s, x, topk_idx, offsets, x_perm, x_perm_scale, perm_token, inv_pos, ws,
@@ -307,7 +310,7 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x_perm, const 
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!tok(x_perm, s) || !tok(x, s) || !offsets || !w_gate_up || !w_down || !tok(y, s)) return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && (!tok(x_perm_scale, s) || !w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(s.dtype) && (!tok(x_perm_scale, s) || !w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
     return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
@@ -323,7 +326,8 @@ moe_status_t moe_expert_ffn_gather(const moe_shape_t* shape, const void* x, cons
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!tok(x, s) || !tok(perm_token, s) || !offsets || !w_gate_up || !w_down || !tok(y, s)) return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (s.dtype == MOE_FP8_E4M3_POW2) return MOE_ERR_UNSUPPORTED;  // block-scaled GEMM: permuted copy only
+  if (is_fp8(s.dtype) && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_ws(s, ws, ws_bytes));
   return launch_expert_ffn(s, nullptr, nullptr, x, perm_token, offsets, w_gate_up, w_gu_scale, w_down,
@@ -358,7 +362,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
   MOE_TRY(validate_shape(shape));
   const moe_shape_t& s = *shape;
   if (!tok(x, s) || !w_router || !bias || !w_gate_up || !w_down || !tok(out, s)) return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(s.dtype) && (!w_gu_scale || !w_down_scale)) return MOE_ERR_INVALID_ARG;
   if (update_bias && (!(gamma >= 0.0f) || gamma > 1.0f)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
     return MOE_ERR_ALIGNMENT;
@@ -382,7 +386,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, const void* x, const void* w_
                               ws, st));
   } else {
     void* xp = w + L.x_perm;
-    float* xps = s.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(w + L.x_perm_scale) : nullptr;
+    float* xps = is_fp8(s.dtype) ? reinterpret_cast<float*>(w + L.x_perm_scale) : nullptr;
     MOE_TRY(launch_permute(s, x, idx, off, xp, xps, ptok, inv, ws, st));
     MOE_TRY(launch_expert_ffn(s, xp, xps, x, nullptr, off, w_gate_up, w_gu_scale, w_down, w_down_scale, y, ws,
                               st));
@@ -405,7 +409,18 @@ moe_status_t moe_quantize_weights_fp8(int G, int N, int K, const void* w, void* 
   if (G == 0 || N == 0 || K == 0) return MOE_OK;
   if (!w || !w_q || !w_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(w_q)) return MOE_ERR_ALIGNMENT;
-  return launch_quant_weights(G, N, K, w, w_q, w_scale, (cudaStream_t)stream);
+  return launch_quant_weights(G, N, K, w, w_q, w_scale, false, (cudaStream_t)stream);
+}
+
+moe_status_t moe_quantize_weights_fp8_pow2(int G, int N, int K, const void* w, void* w_q, float* w_scale,
+                                           moe_stream_t stream) {
+  NvtxRange nvtx_range("moe_quantize_weights_fp8_pow2");
+  if (G < 0 || N < 0 || K < 0 || N % 128 || K % 128) return MOE_ERR_INVALID_ARG;
+  if ((long long)G * N * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if (G == 0 || N == 0 || K == 0) return MOE_OK;
+  if (!w || !w_q || !w_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(w_q)) return MOE_ERR_ALIGNMENT;
+  return launch_quant_weights(G, N, K, w, w_q, w_scale, true, (cudaStream_t)stream);
 }
 
 size_t moe_backward_workspace_bytes(const moe_shape_t* shape) {

@@ -89,7 +89,9 @@ __global__ void bias_update_kernel(const int32_t* __restrict__ counts, float* __
   bias[i] = bias[i] + gamma * sgn;
 }
 
-// one CTA per 128x128 block of one expert matrix
+// one CTA per 128x128 block of one expert matrix; scale = amax / 448, or (POW2) the
+// smallest power of two with amax <= 448 * scale
+template <bool POW2>
 __global__ void __launch_bounds__(256)
     quant_weight_kernel(const uint16_t* __restrict__ w, uint8_t* __restrict__ wq, float* __restrict__ ws, int N,
                         int K) {
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(256)
   amax = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-  const float scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  const float scale = POW2 ? pow2_scale(amax) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
   uint2* dst = reinterpret_cast<uint2*>(wq + base + (size_t)r * K + h * 64);
 #pragma unroll
   for (int v = 0; v < 8; ++v) {
@@ -150,11 +152,16 @@ moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, flo
   return cuda_status(cudaGetLastError());
 }
 
-moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale, cudaStream_t st) {
+moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale, bool pow2,
+                                  cudaStream_t st) {
   if (N / 128 > 65535 || G > 65535) return MOE_ERR_UNSUPPORTED;
   dim3 grid(K / 128, N / 128, G);
-  quant_weight_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint8_t*>(w_q), w_scale,
-                                            N, K);
+  if (pow2)
+    quant_weight_kernel<true><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint8_t*>(w_q),
+                                                    w_scale, N, K);
+  else
+    quant_weight_kernel<false><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint8_t*>(w_q),
+                                                     w_scale, N, K);
   return cuda_status(cudaGetLastError());
 }
 

@@ -76,7 +76,7 @@ extern "C" MOE_API moe_status_t moe_expert_ffn_static(const moe_shape_t* shape, 
   const bool none = s.T == 0;  // no tokens: the token-sized buffers may be NULL
   if (!(x_perm || none) || !(x || none) || !offsets || !w_gate_up || !w_down || !(y || none))
     return MOE_ERR_INVALID_ARG;
-  if (s.dtype == MOE_FP8_E4M3 && (!(x_perm_scale || none) || !w_gu_scale || !w_down_scale))
+  if (moe::is_fp8(s.dtype) && (!(x_perm_scale || none) || !w_gu_scale || !w_down_scale))
     return MOE_ERR_INVALID_ARG;
   if (!moe::aligned16(x_perm) || !moe::aligned16(x) || !moe::aligned16(w_gate_up) || !moe::aligned16(w_down) ||
       !moe::aligned16(y))

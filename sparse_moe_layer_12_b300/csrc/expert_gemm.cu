@@ -587,6 +587,11 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
   if (s.dtype == MOE_FP8_E4M3)
     return launch_expert_ffn_fp8(s, x_perm, x_perm_scale, x, perm_token, offsets, w_gate_up, w_gu_scale, w_down,
                                  w_down_scale, y, ws, st, layout);
+  if (s.dtype == MOE_FP8_E4M3_POW2) {
+    if (perm_token) return MOE_ERR_UNSUPPORTED;  // whole-tile loads of the permuted copy only
+    return launch_expert_ffn_mx(s, x_perm, x_perm_scale, x, offsets, w_gate_up, w_gu_scale, w_down, w_down_scale,
+                                y, ws, st, layout);
+  }
   const bool gather = perm_token != nullptr;
   const WsLayout L = layout ? *layout : ws_layout(s);
   char* w = static_cast<char*>(ws);

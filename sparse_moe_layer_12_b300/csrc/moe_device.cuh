@@ -399,6 +399,44 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
                : "memory");
 }
 
+// ---------------------------------------------------------------- block-scaled E4M3 MMA
+
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scale factors: B scale-factor id
+// (bits 4-5), A and B E4M3 (format 0, bits 7-9 / 10-12), K-major operands, N >> 3 (bits
+// 17-22), scale format UE8M0 (bit 23), M >> 4 (bits 24-28), A scale-factor id (29-30).
+// The scale-factor id picks the byte of the 32-bit TMEM scale words: the 32-wide K
+// sub-block of the instruction within the 128-wide K block.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
+// M = 256 block-scaled MMA over the CTA pair (operands as mma_bf16_pair).  Scale
+// factors live in TMEM: sfa_tmem holds each CTA's own 128 A rows, sfb_tmem the scales
+// of all N B rows in both CTAs; a scale of row n sits in lane n % 32 (every lane
+// quadrant holds the same), column n / 32 (+4 per further 128 rows), byte = K
+// sub-block.
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns from registers (thread i: lane lane_base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ---------------------------------------------------------------- small math
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
@@ -412,17 +450,34 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Power-of-two scale of a tile with absolute maximum amax: the smallest 2^e with
+// amax <= 448 * 2^e (so amax / scale lies in (224, 448]), decided exactly on the bits:
+// amax = (1 + f) 2^E gives e = E - 8, or E - 7 when 1 + f > 1.75 (448 = 1.75 * 2^8).
+// 1 for an all-zero tile; e is kept within [-127, 127], the range of a UE8M0 scale.
+__device__ __forceinline__ float pow2_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  const uint32_t b = __float_as_uint(amax);
+  int e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = e < -127 ? -127 : (e > 127 ? 127 : e);
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// UE8M0 byte of a power-of-two FP32 scale: its biased exponent (2^-127, the one
+// subnormal scale, has exponent field 0 = UE8M0 2^-127 as well).
+__device__ __forceinline__ uint32_t ue8m0_of(float pow2) { return (__float_as_uint(pow2) >> 23) & 0xFFu; }
+
 // One 1x128 E4M3 tile held by 16 consecutive lanes (8 values each, lanes 0-15 or
 // 16-31 of a warp; every lane of the warp must call it): scale = amax / 448 in
-// FP32 (1 for an all-zero tile), codes = RNE_sat(v / scale).  Returns the scale
-// and this lane's 8 codes packed in q.
+// FP32 (POW2: the power of two of pow2_scale), 1 for an all-zero tile, codes =
+// RNE_sat(v / scale).  Returns the scale and this lane's 8 codes packed in q.
+template <bool POW2 = false>
 __device__ __forceinline__ float quant_tile16(const float (&f)[8], uint2& q) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
   for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  const float scale = POW2 ? pow2_scale(amax) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
   uint32_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));

@@ -17,6 +17,7 @@ constexpr int kMaxS = 8;
 constexpr int kMaxK = 16;
 constexpr int kRouterTileM = 128;  // tokens per router tile
 constexpr int kChunkMax = 256;     // tokens per expert-GEMM tile (tcgen05 N)
+constexpr int kChunkMxMax = 224;   // tokens per tile of the block-scaled FP8 GEMM (TMEM also holds scales)
 constexpr int kBoxRows = 32;       // token rows per TMA box in the expert GEMM
 constexpr size_t kForwardGatherMaxRows = 4096;  // moe_forward gathers routed rows while T*k <= this
 
@@ -72,6 +73,8 @@ size_t bwd_kcap(const moe_shape_t& s);
 BwdLayout bwd_layout(const moe_shape_t& s);
 
 bool shape_valid(const moe_shape_t* s);
+// E4M3 activations and weights with 1x128 / 128x128 scales (FP32 scales, or powers of two)
+inline bool is_fp8(moe_dtype_t t) { return t == MOE_FP8_E4M3 || t == MOE_FP8_E4M3_POW2; }
 bool forward_gathers(const moe_shape_t& s);  // moe_forward's dispatch form (see moe_forward_gathers)
 WsLayout ws_layout(const moe_shape_t& s);
 // The expert FFN's scratch alone (status word, schedule, FP8 copy of x and its scales,
@@ -122,6 +125,11 @@ moe_status_t launch_expert_ffn_fp8(const moe_shape_t& s, const void* x_perm, con
                                    const void* w_gate_up, const float* w_gu_scale, const void* w_down,
                                    const float* w_down_scale, void* y, void* ws, cudaStream_t st,
                                    const WsLayout* layout = nullptr);
+// block-scaled E4M3 expert FFN (power-of-two scales; csrc/expert_gemm_mx.cu); routed rows from x_perm
+moe_status_t launch_expert_ffn_mx(const moe_shape_t& s, const void* x_perm, const float* x_perm_scale, const void* x,
+                                  const int32_t* offsets, const void* w_gate_up, const float* w_gu_scale,
+                                  const void* w_down, const float* w_down_scale, void* y, void* ws, cudaStream_t st,
+                                  const WsLayout* layout = nullptr);
 // per-group token counts, chunking (<= chunk_max tokens) and tile prefix sums (one block of 512 threads)
 __global__ void schedule_kernel(const int32_t* __restrict__ offsets, int T, int k, int E, int S, int m_gu, int m_dn,
                                 int chunk_max, GroupInfo* __restrict__ groups, int* __restrict__ ts_gu,
@@ -150,7 +158,7 @@ moe_status_t launch_combine(const moe_shape_t& s, const void* y, const float* ga
                             void* out, cudaStream_t st);
 moe_status_t launch_bias_update(const moe_shape_t& s, const int32_t* counts, float* bias, float gamma,
                                 cudaStream_t st);
-moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale,
+moe_status_t launch_quant_weights(int G, int N, int K, const void* w, void* w_q, float* w_scale, bool pow2,
                                   cudaStream_t st);
 moe_status_t launch_debug_wait(void* ws, unsigned limit_us, cudaStream_t st);
 // expert parallelism: rows between source-major and local expert-major order (csrc/ep.cu)

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kRankThreads)
   if (tid == 0 && running != hi - lo) set_error(status, status + 1, MOE_ERR_DEVICE, kSitePermute);
 }
 
-template <bool FP8>
+template <bool FP8, bool POW2 = false>
 __global__ void __launch_bounds__(kScatterThreads)
     permute_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos, int T, int d, int k,
                            uint8_t* __restrict__ x_perm, float* __restrict__ x_perm_scale, int* __restrict__ status) {
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kScatterThreads)
       if (valid) raw = __ldg(xr + v);
       bf16x8_to_f32(raw, f);
       uint2 q;
-      const float scale = quant_tile16(f, q);
+      const float scale = quant_tile16<POW2>(f, q);
       if (valid) {
         const int tile = v >> 4;
         for (int j = 0; j < k; ++j) {
@@ -141,6 +141,9 @@ moe_status_t launch_permute(const moe_shape_t& s, const void* x, const int32_t* 
   if (x_perm == nullptr) return MOE_OK;  // tables only (the fused forward gathers rows in the GEMM)
   if (s.dtype == MOE_FP8_E4M3)
     permute_scatter_kernel<true><<<s.T, kScatterThreads, 0, st>>>(
+        static_cast<const uint4*>(x), inv_pos, s.T, s.d, s.k, static_cast<uint8_t*>(x_perm), x_perm_scale, status);
+  else if (s.dtype == MOE_FP8_E4M3_POW2)
+    permute_scatter_kernel<true, true><<<s.T, kScatterThreads, 0, st>>>(
         static_cast<const uint4*>(x), inv_pos, s.T, s.d, s.k, static_cast<uint8_t*>(x_perm), x_perm_scale, status);
   else
     permute_scatter_kernel<false><<<s.T, kScatterThreads, 0, st>>>(

@@ -38,6 +38,7 @@ class MoEConfig:
     bias_uniform: float = 0.0  # b ~ U(-a, a); 0 -> b = 0
     zipf_amp: float = 0.0  # logit offsets A * r^-1.1; 0 -> none
     fp8: bool = False
+    pow2: bool = False  # FP8 with power-of-two block scales
     n_group: int = 0  # group-limited routing: groups of experts (0 = none)
     topk_group: int = 0  # groups kept per token
     seed: int = 0
@@ -68,6 +69,8 @@ CONFIGS: dict[str, MoEConfig] = {
     "v3": MoEConfig("v3", 8192, 7168, 256, 1, 8, 2048, 0.006),
     # V3-shaped FP8 path: T=16384
     "v3fp8": MoEConfig("v3fp8", 16384, 7168, 256, 1, 8, 2048, 0.006, fp8=True),
+    # the same with power-of-two block scales (applied by the block-scaled tensor-core MMA)
+    "v3fp8p2": MoEConfig("v3fp8p2", 16384, 7168, 256, 1, 8, 2048, 0.006, fp8=True, pow2=True),
     # V3 shape with group-limited routing: 8 groups of 32 experts, 4 groups per token
     "v3grp": MoEConfig("v3grp", 8192, 7168, 256, 1, 8, 2048, 0.006, n_group=8, topk_group=4),
     # skewed-load decode regime: T=256 with Zipf(1.1) logit offsets, amplitude 2.0
@@ -158,22 +161,27 @@ def make_experts(cfg: MoEConfig, device="cpu") -> tuple[torch.Tensor, torch.Tens
 _ID_WGU8, _ID_WD8 = 7, 8
 
 
-def make_expert_fp8(cfg: MoEConfig, e: int, device="cpu"):
+def make_expert_fp8(cfg: MoEConfig, e: int, device="cpu", pow2: bool = False):
     """FP8 weights of expert e drawn directly (not quantised from bf16): E4M3 codes of
     N(0, 64) values (torch's float8_e4m3fn cast) and per-128x128-block scales around
-    1/(64 sqrt(fan_in)), so that code * scale ~ N(0, 1/sqrt(fan_in)).
+    1/(64 sqrt(fan_in)), so that code * scale ~ N(0, 1/sqrt(fan_in)); pow2: scales drawn
+    from the two powers of two 2^-(p + b), p = round(log2(64 sqrt(fan_in))), b in {0, 1}.
     Returns (wgu_q [2I, d], wgu_scale [2I/128, d/128], wd_q [d, I], wd_scale [d/128, I/128])."""
     out = []
     for tid, (n, k) in ((_ID_WGU8, (2 * cfg.I, cfg.d)), (_ID_WD8, (cfg.d, cfg.I))):
         g = _gen(device, cfg.seed, tid, e)
         q = (torch.randn(n, k, generator=g, device=device) * 64.0).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         u = torch.rand(n // 128, k // 128, generator=g, device=device)
-        sc = (0.5 + u) / (64.0 * math.sqrt(k))
+        if pow2:
+            p = round(math.log2(64.0 * math.sqrt(k)))
+            sc = torch.exp2(-(p + (u < 0.5).to(torch.float32)))
+        else:
+            sc = (0.5 + u) / (64.0 * math.sqrt(k))
         out += [q, sc.to(torch.float32)]
     return tuple(out)
 
 
-def make_experts_fp8(cfg: MoEConfig, device="cpu"):
+def make_experts_fp8(cfg: MoEConfig, device="cpu", pow2: bool = False):
     """All E+S experts in FP8: (wgu_q [E+S, 2I, d], wgu_scale, wd_q [E+S, d, I], wd_scale)."""
     n = cfg.E + cfg.S
     wgu = torch.empty(n, 2 * cfg.I, cfg.d, dtype=torch.float8_e4m3fn, device=device)
@@ -181,7 +189,7 @@ def make_experts_fp8(cfg: MoEConfig, device="cpu"):
     wd = torch.empty(n, cfg.d, cfg.I, dtype=torch.float8_e4m3fn, device=device)
     ds = torch.empty(n, cfg.d // 128, cfg.I // 128, dtype=torch.float32, device=device)
     for e in range(n):
-        a, b, c, d_ = make_expert_fp8(cfg, e, device)
+        a, b, c, d_ = make_expert_fp8(cfg, e, device, pow2)
         wgu[e].copy_(a)
         gs[e].copy_(b)
         wd[e].copy_(c)

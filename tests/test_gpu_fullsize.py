@@ -60,7 +60,7 @@ def _shared_rows(T):
 
 def _run_layer(cfg, x, wr, b, wgu, wd, gs=None, ds=None):
     fp8 = gs is not None
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8, pow2=cfg.pow2)
     assert not B.forward_gathers(s), "the benchmark's dispatch form at this size is the permuted copy"
     ws = B.alloc_workspace(s)
     idx, gate, counts, offsets = B.moe_route(s, x, wr, b, ws=ws)
@@ -133,14 +133,17 @@ def test_v3_bf16_whole_experts_and_output(libmoe):
     assert r["out_err"] < TOL_MAX and r["fro"] < TOL_FRO
 
 
-def test_v3_fp8_whole_experts_and_output(libmoe):
-    cfg = I.CONFIGS["v3fp8"]
+@pytest.mark.parametrize("name", ["v3fp8", "v3fp8p2"])
+def test_v3_fp8_whole_experts_and_output(libmoe, name):
+    # v3fp8: FP32 block scales; v3fp8p2: power-of-two block scales (block-scaled MMA)
+    cfg = I.CONFIGS[name]
+    p2 = cfg.pow2
     x, wr, b = I.make_x(cfg, DEV), I.make_router(cfg, DEV), I.make_bias(cfg, DEV)
-    wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV)
+    wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV, pow2=p2)
     idx, gate, counts, offsets, ptok, y, out = _run_layer(cfg, x, wr, b, wgu, wd, gs, ds)
     ref = oracle_route(x, wr, b, cfg.k)
     ties = check_routing(ref, idx, gate, counts, offsets, cfg.E)
-    print(f"v3fp8: near-tied tokens {ties}")
+    print(f"{name}: near-tied tokens {ties}")
 
     def u8(t):
         return t.view(torch.uint8).cpu().numpy()
@@ -155,8 +158,8 @@ def test_v3_fp8_whole_experts_and_output(libmoe):
         return getall(e)[0]
 
     experts = _pick_experts(counts.cpu().numpy(), np.random.default_rng(0))
-    _check_whole_experts(cfg, x, ptok, offsets, y, experts, lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e)),
-                         max_tol=TOL_MAX_FP8)
+    _check_whole_experts(cfg, x, ptok, offsets, y, experts,
+                         lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e), pow2=p2), max_tol=TOL_MAX_FP8)
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     tok = np.sort(np.random.default_rng(1).choice(clean, size=256, replace=False))
     xn = np64(x)
@@ -169,12 +172,12 @@ def test_v3_fp8_whole_experts_and_output(libmoe):
         rows, slot = (np.arange(tok.size), None) if e >= cfg.E else np.nonzero(sel == e)
         w = 1.0 if slot is None else g[rows, slot][:, None]
         q, wgu_e, wd_e = getall(e)
-        yq[rows] += w * Q.fp8_swiglu_expert(xs[rows], *q)
+        yq[rows] += w * Q.fp8_swiglu_expert(xs[rows], *q, pow2=p2)
         yu[rows] += w * O.swiglu_expert(xs[rows], wgu_e, wd_e)
     o = np64(out)[tok]
     r = errs(o, yq)
-    _report("v3fp8 layer output vs the oracle's FP8 layer (256 tokens)", r)
+    _report(f"{name} layer output vs the oracle's FP8 layer (256 tokens)", r)
     ru = errs(o, yu)
-    _report("v3fp8 layer output vs the unquantised layer (256 tokens)", ru)
+    _report(f"{name} layer output vs the unquantised layer (256 tokens)", ru)
     assert r["out_err"] < TOL_MAX_FP8 and r["fro"] < TOL_FRO
     assert ru["fro"] < TOL_FRO_FP8_UNQUANTISED

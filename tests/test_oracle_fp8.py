@@ -181,3 +181,73 @@ def test_fp8_expert_h_rounding_is_visible():
     y_exact_h = h @ wd.T
     rel = np.abs(y - y_exact_h) / np.maximum(np.abs(y_exact_h), 1e-30)
     assert rel.max() > 1e-2
+
+
+# ---- power-of-two scales (the smallest 2^e with amax <= 448 * 2^e)
+
+
+def test_pow2_scale_closed_forms():
+    eps = np.float32(2.0 ** -23)
+    cases = [
+        (448.0, 1.0),                      # amax = 448 exactly: scale 1, code 448
+        (448.0 * (1 + eps), 2.0),          # one ulp above: the next power
+        (224.0, 0.5),                      # 224 / 0.5 = 448
+        (224.0 * (1 + eps), 1.0),
+        (1.75, 2.0 ** -8),                 # 1.75 / 448 = 2^-8 exactly
+        (1.75 * (1 + eps), 2.0 ** -7),
+        (1.0, 2.0 ** -8),                  # 1 / 448 lies between 2^-9 and 2^-8
+        (0.0, 1.0),                        # empty tile
+        (448.0 * 2.0 ** 100, 2.0 ** 100),
+        (1e-38, 2.0 ** -127),              # below 448 * 2^-127: the smallest one-byte scale
+    ]
+    amax = np.array([a for a, _ in cases], dtype=np.float32)
+    got = Q.pow2_scale(amax)
+    np.testing.assert_array_equal(got, np.array([s for _, s in cases], dtype=np.float32))
+
+
+def test_pow2_scale_puts_the_tile_max_in_224_448():
+    rng = np.random.default_rng(5)
+    amax = (np.exp(rng.uniform(-60, 60, 100_000)) * rng.uniform(0.5, 1.0, 100_000)).astype(np.float32)
+    sc = Q.pow2_scale(amax)
+    m, _ = np.frexp(sc.astype(np.float64))
+    assert np.all(m == 0.5)  # powers of two
+    r = amax.astype(np.float64) / sc.astype(np.float64)
+    assert np.all(r <= 448.0) and np.all(r > 224.0)
+
+
+def test_pow2_tiles_codes_match_torch():
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((9, 384)) * np.exp(rng.uniform(-8, 8, (9, 1)))).astype(np.float32)
+    x[3, 128:256] = 0.0
+    q, sc = Q.quantize_act_1x128(x, pow2=True)
+    for r in range(9):
+        for b in range(3):
+            tile = x[r, b * 128:(b + 1) * 128]
+            s = np.float32(sc[r, b])
+            want = torch.from_numpy(tile / s).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(q[r, b * 128:(b + 1) * 128], want)
+            if np.abs(tile).max() > 0:
+                assert 224.0 <= np.abs(Q.e4m3_decode(q[r, b * 128:(b + 1) * 128])).max() <= 448.0
+    wq, wsc = Q.quantize_weight_128x128(x[:, :256].repeat(128 // 9 + 1, axis=0)[:128], pow2=True)
+    m, _ = np.frexp(wsc.astype(np.float64))
+    assert np.all(m == 0.5)
+
+
+def test_fp8_expert_pow2_quantises_h_per_1x128_along_I():
+    # the hand case above with power-of-two activation scales: h's tile scale is the
+    # power of two above amax / 448 and its codes are torch's E4M3 cast of h / scale
+    x, x0, up, wgu_q, wgu_sc, wd_q, wd_sc = _h_quant_case()
+    y = Q.fp8_swiglu_expert(x, wgu_q, wgu_sc, wd_q, wd_sc, pow2=True)
+    for t in range(2):
+        a = 0.25 * x0[t]
+        silu_a = float(torch.nn.functional.silu(torch.tensor(a, dtype=torch.float64)))
+        h = (silu_a * 0.25 * x0[t] * up).astype(np.float32)
+        hq = np.zeros(256)
+        for tile in range(2):
+            seg = h[tile * 128:(tile + 1) * 128]
+            amax = float(np.abs(seg).max())
+            m, ex = np.frexp(amax)  # the power of two above amax / 448, restated
+            s = 2.0 ** (ex - 9 if m <= 0.875 else ex - 8)
+            codes = torch.from_numpy((seg / np.float32(s)).astype(np.float32)).to(torch.float8_e4m3fn)
+            hq[tile * 128:(tile + 1) * 128] = codes.double().numpy() * s
+        np.testing.assert_allclose(y[t], hq[:128] + hq[128:], rtol=1e-12, atol=0)
