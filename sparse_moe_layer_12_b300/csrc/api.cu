@@ -72,6 +72,10 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.h = o;           o = align_up(o + rows * s.I * es, A);
   L.h_scale = o;     o = align_up(o + (f8 ? rows * (s.I / 128) * 4 : 0), A);
   L.y = o;           o = align_up(o + rows * s.d * 2, A);
+  const bool p2 = s.dtype == MOE_FP8_E4M3_POW2;
+  L.sb_xp = o;       o = align_up(o + (p2 ? Tk * (s.d / 128) : 0), A);
+  L.sb_xq = o;       o = align_up(o + (p2 ? (size_t)s.T * (s.d / 128) : 0), A);
+  L.sb_h = o;        o = align_up(o + (p2 ? rows * (s.I / 128) : 0), A);
   L.total = o;
   return L;
 }
@@ -88,6 +92,10 @@ WsLayout ffn_ws_layout(const moe_shape_t& s) {
   L.xq_scale = o;    o = align_up(o + (f8 ? (size_t)s.T * (s.d / 128) * 4 : 0), A);
   L.h = o;           o = align_up(o + rows * s.I * (f8 ? 1 : 2), A);
   L.h_scale = o;     o = align_up(o + (f8 ? rows * (s.I / 128) * 4 : 0), A);
+  const bool p2 = s.dtype == MOE_FP8_E4M3_POW2;
+  L.sb_xp = o;       o = align_up(o + (p2 ? (size_t)s.T * s.k * (s.d / 128) : 0), A);
+  L.sb_xq = o;       o = align_up(o + (p2 ? (size_t)s.T * (s.d / 128) : 0), A);
+  L.sb_h = o;        o = align_up(o + (p2 ? rows * (s.I / 128) : 0), A);
   L.total = o;
   return L;
 }
@@ -215,6 +223,41 @@ bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
   cuuint32_t box[3] = {box_inner, box_mid, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return f(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weight view that fetches the two 128-row A blocks of an expert-GEMM tile in one load:
+// dims {K, rows, 2, groups} with the "2" dimension `gap` rows apart (gate/up: the up rows
+// are I rows after the gate rows; group g = one expert, g_stride rows apart), box
+// {box_k, 128, 2, 1}, 128-byte swizzle.  The two blocks land one after the other.
+bool make_map_pair_rows(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K,
+                        uint64_t rows, uint64_t gap, uint64_t groups, uint64_t g_stride, uint32_t box_k) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || !aligned16(base)) return false;
+  cuuint64_t dims[4] = {K, rows, 2, groups};
+  cuuint64_t strides[3] = {K * (uint64_t)esize, gap * K * (uint64_t)esize, g_stride * K * (uint64_t)esize};
+  cuuint32_t box[4] = {box_k, 128, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return f(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// As make_map_pair_rows with a further dimension: {K, rows, 2, blocks, groups}, the "2"
+// dimension `gap` rows apart, `blocks` of `b_stride` rows (W_down: channel blocks 0 and 1 of
+// a 512-channel tile, 256 rows apart, tiles 512 rows apart).
+bool make_map_pair_rows5(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K,
+                         uint64_t rows, uint64_t gap, uint64_t blocks, uint64_t b_stride, uint64_t groups,
+                         uint64_t g_stride, uint32_t box_k) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || !aligned16(base)) return false;
+  const uint64_t rb = K * (uint64_t)esize;
+  cuuint64_t dims[5] = {K, rows, 2, blocks, groups};
+  cuuint64_t strides[4] = {rb, gap * rb, b_stride * rb, g_stride * rb};
+  cuuint32_t box[5] = {box_k, 128, 2, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return f(m, dt, 5, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

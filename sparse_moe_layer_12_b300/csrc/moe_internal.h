@@ -57,6 +57,9 @@ struct Schedule {
 struct WsLayout {
   size_t status, counts, offsets, idx, gate, perm_token, inv_pos, sched;
   size_t x_perm, x_perm_scale, xq, xq_scale, h, h_scale, y;
+  // power-of-two FP8 only: UE8M0 bytes of the token scales, K-block major ([K/128][rows])
+  // for the routed rows of x_perm, the shared experts' rows of x and the rows of h
+  size_t sb_xp, sb_xq, sb_h;
   size_t total;
 };
 
@@ -102,6 +105,13 @@ bool make_map_3d_sw64(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
                       uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
 bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
                  uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid);
+// the two 128-row A blocks of a tile in one load (see api.cu): 4-D {K, rows, 2, groups} and
+// 5-D {K, rows, 2, blocks, groups}
+bool make_map_pair_rows(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K,
+                        uint64_t rows, uint64_t gap, uint64_t groups, uint64_t g_stride, uint32_t box_k);
+bool make_map_pair_rows5(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K,
+                         uint64_t rows, uint64_t gap, uint64_t blocks, uint64_t b_stride, uint64_t groups,
+                         uint64_t g_stride, uint32_t box_k);
 
 // launchers (each returns MOE_OK or MOE_ERR_CUDA); pointers already validated
 moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_router, const float* bias,
