@@ -140,6 +140,7 @@ template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b0,
                        const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_xg,
+                       const __grid_constant__ CUtensorMap map_wp, int a_pair,
                        const GroupInfo* __restrict__ groups, const int* __restrict__ tile_start, int G, int E, int K,
                        int I, int d, const int32_t* __restrict__ perm_token, int x_rows,
                        uint16_t* __restrict__ out, uint16_t* __restrict__ out2, int* __restrict__ status) {
@@ -209,8 +210,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nm = (ti.n + 15) & ~15;
       const int half = nm / 2;  // token rows per CTA (multiple of 8)
       const bool gat = !ti.shared_b;
-      const int nbox_mine = gat ? 0 : (half + kBoxRows - 1) / kBoxRows;
-      const uint32_t b_mine = gat ? half * 128u : nbox_mine * kBox;
+      // shared experts' contiguous rows: one 128-row box
+      const uint32_t b_mine = gat ? half * 128u : kBTile;
       const uint32_t bytes_pair = 2 * (2 * kATile + b_mine);  // both CTAs (same row count)
       const int a0_row = ti.mp * 256 + rank * 128;  // gate rows of this CTA's 128 features
       const int a1_row = I + a0_row;                // up rows of the same features
@@ -244,10 +245,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int kq = (kb + ti.mp * kKStagger) % nk;
         if (lane == 0) {
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes_pair);
-          tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, ti.expert);
-          tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, ti.expert);
-          for (int b = 0; b < nbox_mine; ++b)
-            tma_load_2d_pair(st + 2 * kATile + b * kBox, &map_b1, fb, kq * 64, brow + b * kBoxRows);
+          if (a_pair) {
+            tma_load_4d_pair(st, &map_wp, fb, kq * 64, a0_row, 0, ti.expert);
+          } else {
+            tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, ti.expert);
+            tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, ti.expert);
+          }
+          if (!gat) tma_load_2d_pair(st + 2 * kATile, &map_b1, fb, kq * 64, brow);
           last_round[s] = r;
         }
         if (my_rows)
@@ -266,9 +270,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nk = ti.nk >= 0 ? ti.nk : nk_all;
         const int nm = (ti.n + 15) & ~15;
         const int half = nm / 2;  // token rows per CTA (multiple of 8)
-        // token operand: 32-row K-major boxes, or (weight gradient) 64-column MN-major boxes
-        const int nbox_mine = MODE == kWgrad ? half / 64 : (half + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes_pair = 2 * (2 * kATile + nbox_mine * (MODE == kWgrad ? 8192u : kBox));
+        // token operand: one 128-row K-major box (forward), 32-row K-major boxes, or (weight
+        // gradient) 64-column MN-major boxes
+        constexpr bool kFwd = MODE == kGateUp || MODE == kDown;
+        const int nbox_mine = kFwd ? 1 : MODE == kWgrad ? half / 64 : (half + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes_pair =
+            2 * (2 * kATile + (kFwd ? kBTile : nbox_mine * (MODE == kWgrad ? 8192u : kBox)));
         int a0_row, a1_row;
         if (MODE == kGateUp || MODE == kGateUpRaw) {
           a0_row = ti.mp * 256 + rank * 128;        // gate rows of this CTA's 128 features
@@ -296,11 +303,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_3d_pair(st + 8192, &map_w, fb, a0_row + 64, kq * 64, wexp);
             tma_load_3d_pair(st + kATile, &map_w, fb, a1_row, kq * 64, wexp);
             tma_load_3d_pair(st + kATile + 8192, &map_w, fb, a1_row + 64, kq * 64, wexp);
+          } else if (kFwd && a_pair == 1) {  // gate and up blocks: {K, I rows, gate/up, expert}
+            tma_load_4d_pair(st, &map_wp, fb, kq * 64, a0_row, 0, wexp);
+          } else if (kFwd && a_pair == 2) {  // channel blocks 0 and 1: {K, 256 rows, block, tile, expert}
+            tma_load_5d_pair(st, &map_wp, fb, kq * 64, static_cast<int>(rank) * 128, 0, ti.mp, wexp);
           } else {
             tma_load_3d_pair(st, &map_w, fb, kq * 64, a0_row, wexp);
             tma_load_3d_pair(st + kATile, &map_w, fb, kq * 64, a1_row, wexp);
           }
-          if (MODE == kWgrad) {
+          if (kFwd) {
+            tma_load_2d_pair(st + 2 * kATile, mb, fb, kq * 64, brow);
+          } else if (MODE == kWgrad) {
             for (int b = 0; b < nbox_mine; ++b)
               tma_load_2d_pair(st + 2 * kATile + b * 8192, mb, fb, brow + b * 64, kq * 64);
           } else {
@@ -610,19 +623,28 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
                                      status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
-  CUtensorMap m_wgu, m_xp, m_x, m_xg, m_wd, m_h;
+  CUtensorMap m_wgu, m_wgu_p, m_xp, m_x, m_xg, m_wd, m_wd_p, m_h;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map_3d(&m_wgu, w_gate_up, bf, 2, s.d, 2 * (uint64_t)s.I, G, 64, 128)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_x, x, bf, 2, s.d, s.T, 64, kBoxRows)) return MOE_ERR_CUDA;
+  // gate and up rows of a tile in one load: the up block is I rows after the gate block
+  if (!make_map_pair_rows(&m_wgu_p, w_gate_up, bf, 2, s.d, s.I, s.I, G, 2 * (uint64_t)s.I, 64))
+    return MOE_ERR_CUDA;
+  // token rows: one 128-row box per stage (this CTA's half of <= 256 rows)
+  if (!make_map_2d(&m_x, x, bf, 2, s.d, s.T, 64, 128)) return MOE_ERR_CUDA;
   if (gather) {  // routed rows gathered from x one row at a time; no permuted copy
     if (!make_map_2d(&m_xg, x, bf, 2, s.d, s.T, 64, 1)) return MOE_ERR_CUDA;
     m_xp = m_x;
   } else {
-    if (!make_map_2d(&m_xp, x_perm, bf, 2, s.d, Tk, 64, kBoxRows)) return MOE_ERR_CUDA;
+    if (!make_map_2d(&m_xp, x_perm, bf, 2, s.d, Tk, 64, 128)) return MOE_ERR_CUDA;
     m_xg = m_x;
   }
   if (!make_map_3d(&m_wd, w_down, bf, 2, s.I, s.d, G, 64, 128)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_h, h, bf, 2, s.I, rows, 64, kBoxRows)) return MOE_ERR_CUDA;
+  // the two channel blocks of a 512-channel tile in one load (when d is a multiple of 512)
+  const int dn_pair = s.d % 512 == 0 ? 2 : 0;
+  m_wd_p = m_wd;
+  if (dn_pair && !make_map_pair_rows5(&m_wd_p, w_down, bf, 2, s.I, 256, 256, s.d / 512, 512, G, s.d, 64))
+    return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_h, h, bf, 2, s.I, rows, 64, 128)) return MOE_ERR_CUDA;
 
   auto k_gu = gather ? expert_gemm_kernel<kGateUp, true> : expert_gemm_kernel<kGateUp, false>;
   auto k_dn = expert_gemm_kernel<kDown, false>;
@@ -632,11 +654,11 @@ moe_status_t launch_expert_ffn(const moe_shape_t& s, const void* x_perm, const f
     return MOE_ERR_CUDA;
   const int grid = pair_grid((const void*)k_gu, kThreads, kSmemBytes);
   if (grid <= 0) return MOE_ERR_CUDA;
-  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, m_xg, groups, ts_gu, G, s.E, s.d, s.I, s.d, perm_token,
-                                          s.T, h, nullptr, status);
+  k_gu<<<grid, kThreads, kSmemBytes, st>>>(m_wgu, m_xp, m_x, m_xg, m_wgu_p, 1, groups, ts_gu, G, s.E, s.d, s.I, s.d,
+                                          perm_token, s.T, h, nullptr, status);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, m_h, groups, ts_dn, G, s.E, s.I, s.I, s.d, nullptr, 0,
-                                          static_cast<uint16_t*>(y), nullptr, status);
+  k_dn<<<grid, kThreads, kSmemBytes, st>>>(m_wd, m_h, m_h, m_h, m_wd_p, dn_pair, groups, ts_dn, G, s.E, s.I, s.I,
+                                          s.d, nullptr, 0, static_cast<uint16_t*>(y), nullptr, status);
   return cuda_status(cudaGetLastError());
 }
 
@@ -657,13 +679,14 @@ moe_status_t launch_gemm_bwd(GemmMode mode, const CUtensorMap& map_w, const CUte
     return MOE_ERR_CUDA;
   const int grid = pair_grid(fn, kThreads, kSmemBytes);
   if (grid <= 0) return MOE_ERR_CUDA;
-  CUtensorMap mw = map_w, m0 = map_b0, m1 = map_b1, mg = map_out ? *map_out : map_b0;
+  CUtensorMap mw = map_w, m0 = map_b0, m1 = map_b1, mg = map_out ? *map_out : map_b0, mwp = map_w;
+  int a_pair = 0;  // the backward modes load their A blocks one at a time
   const int32_t* no_perm = nullptr;
   int x_rows = 0;
   uint16_t* o = static_cast<uint16_t*>(out);
   uint16_t* o2 = static_cast<uint16_t*>(out2);
-  void* args[] = {&mw, &m0, &m1, &mg, &groups, &tile_start, &G, &E, &K, &I, &width, &no_perm, &x_rows, &o, &o2,
-                  &status};
+  void* args[] = {&mw, &m0, &m1, &mg, &mwp, &a_pair, &groups, &tile_start, &G, &E, &K, &I, &width, &no_perm, &x_rows,
+                  &o, &o2, &status};
   return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, kSmemBytes, st));
 }
 

@@ -11,12 +11,12 @@ Frobenius error, which a dropped term or a wrong index cannot pass.
 
 bf16: out_err <= 2e-2, Frobenius <= 5e-3 (h, y and out are each rounded to bf16
 once: 2^-9 / sqrt(3) RMS relative error each, about 2e-3 together).
-FP8: against the oracle's FP8 layer (same 1x128 / 128x128 quantisation) Frobenius
-<= 5e-3 as bf16, since both sides quantise the same values, and out_err <= 3e-2:
-where h lies within the FP32-vs-float64 difference of a rounding midpoint the two
-sides pick neighbouring E4M3 codes, one step of 32/448 of the tile's amax, which
-reaches an output through a W_down element of up to ~4.5/sqrt(I), 2.8 % of the
-output RMS (measured: 1.8e-2 on one V3 expert); against the layer with
+FP8 (FP32 and power-of-two scales): against the oracle's FP8 layer (same 1x128 /
+128x128 quantisation) the gates of moe_testutil.fp8_ok -- Frobenius <= 5e-3 as bf16,
+at most 1e-4 of the elements beyond the bf16 bound, every element within 0.15 -- since
+an E4M3 code of h that flips at a rounding midpoint moves a handful of a row's outputs
+by up to ~11 % of the RMS (measured: 7.2e-2 on one V3 expert with power-of-two
+scales) while a wrong scale, index or tile moves thousands; against the layer with
 x and h left unquantised the relative Frobenius error must stay below 6e-2 (E4M3's
 three mantissa bits alone cost about 4.4 %, and its max error, 20-30 % of the RMS,
 is reported only).
@@ -29,12 +29,11 @@ from oracle import fp8 as Q
 from oracle import moe_oracle as O
 from sparse_moe_layer_12_b300 import binding as B
 from sparse_moe_layer_12_b300 import inputs as I
-from moe_testutil import check_routing, errs, np64, oracle_route
+from moe_testutil import check_routing, errs, fp8_errs, fp8_ok, np64, oracle_route
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 TOL_MAX = 2e-2
-TOL_MAX_FP8 = 3e-2  # one E4M3 code flip of h (see above)
 TOL_FRO = 5e-3
 TOL_FRO_FP8_UNQUANTISED = 6e-2
 
@@ -77,10 +76,14 @@ def _run_layer(cfg, x, wr, b, wgu, wd, gs=None, ds=None):
 
 
 def _report(tag, e):
-    print(f"{tag}: out_err {e['out_err']:.3e}  max/RMS {e['max_rms']:.3e}  Frobenius {e['fro']:.3e}")
+    extra = f"  beyond the bf16 bound {e['frac_over']:.2e}" if "frac_over" in e else ""
+    print(f"{tag}: out_err {e['out_err']:.3e}  max/RMS {e['max_rms']:.3e}  Frobenius {e['fro']:.3e}{extra}")
 
 
-def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, max_tol=TOL_MAX):
+def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, fp8=False):
+    def ok(e):
+        return fp8_ok(e) if fp8 else (e["out_err"] < TOL_MAX and e["fro"] < TOL_FRO)
+
     xn = np64(x)
     ptok = ptok.cpu().numpy()
     off = offsets.cpu().numpy()
@@ -89,17 +92,17 @@ def _check_whole_experts(cfg, x, ptok, offsets, y, experts, expert_fn, max_tol=T
         lo, hi = int(off[e]), int(off[e + 1])
         want = expert_fn(e, xn[ptok[lo:hi]])
         got = np64(yg[lo:hi])
-        r = errs(got, want)
+        r = fp8_errs(got, want) if fp8 else errs(got, want)
         _report(f"{cfg.name} expert {e} ({hi - lo} tokens)", r)
-        assert r["out_err"] < max_tol and r["fro"] < TOL_FRO, e
+        assert ok(r), e
     Tk = cfg.T * cfg.k
     tok = _shared_rows(cfg.T)
     for si in range(cfg.S):
         want = expert_fn(cfg.E + si, xn[tok])
         got = np64(yg[torch.as_tensor(Tk + si * cfg.T + tok, device=yg.device)])
-        r = errs(got, want)
+        r = fp8_errs(got, want) if fp8 else errs(got, want)
         _report(f"{cfg.name} shared expert {si} ({tok.size} tokens)", r)
-        assert r["out_err"] < max_tol and r["fro"] < TOL_FRO
+        assert ok(r)
 
 
 def _cached(fn):
@@ -159,7 +162,7 @@ def test_v3_fp8_whole_experts_and_output(libmoe, name):
 
     experts = _pick_experts(counts.cpu().numpy(), np.random.default_rng(0))
     _check_whole_experts(cfg, x, ptok, offsets, y, experts,
-                         lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e), pow2=p2), max_tol=TOL_MAX_FP8)
+                         lambda e, rows: Q.fp8_swiglu_expert(rows, *getq(e), pow2=p2), fp8=True)
     clean = np.nonzero(~(ref["boundary_tie"] | ref["order_tie"]))[0]
     tok = np.sort(np.random.default_rng(1).choice(clean, size=256, replace=False))
     xn = np64(x)
@@ -175,9 +178,9 @@ def test_v3_fp8_whole_experts_and_output(libmoe, name):
         yq[rows] += w * Q.fp8_swiglu_expert(xs[rows], *q, pow2=p2)
         yu[rows] += w * O.swiglu_expert(xs[rows], wgu_e, wd_e)
     o = np64(out)[tok]
-    r = errs(o, yq)
+    r = fp8_errs(o, yq)
     _report(f"{name} layer output vs the oracle's FP8 layer (256 tokens)", r)
     ru = errs(o, yu)
     _report(f"{name} layer output vs the unquantised layer (256 tokens)", ru)
-    assert r["out_err"] < TOL_MAX_FP8 and r["fro"] < TOL_FRO
+    assert fp8_ok(r)
     assert ru["fro"] < TOL_FRO_FP8_UNQUANTISED

@@ -58,3 +58,22 @@ def test_group_tie_rejects_a_worse_group():
 def test_fro_err():
     ref = np.array([3.0, 4.0])
     assert fro_err(np.array([3.0, 4.5]), ref) == pytest.approx(0.1)
+
+
+def test_fp8_gates_tell_a_flip_from_a_tile_error():
+    from moe_testutil import fp8_errs, fp8_ok
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((502, 2048))
+    base = ref * (1 + rng.uniform(-2 ** -9, 2 ** -9, ref.shape))  # bf16-level rounding
+    # one E4M3 flip of h: one row moves through a column of W_down (a few large elements)
+    flip = base.copy()
+    w = rng.standard_normal(2048) / np.sqrt(2048)
+    flip[77] += 0.8 * w
+    e = fp8_errs(flip, ref)
+    assert fp8_ok(e), e
+    # a 2 % scale error on one 176-token x 256-feature tile: small in Frobenius, but
+    # thousands of elements beyond the bf16 bound
+    tile = base.copy()
+    tile[176:352, 256:512] *= 1.02
+    e = fp8_errs(tile, ref)
+    assert e["fro"] < 5e-3 and not fp8_ok(e), e
