@@ -113,15 +113,17 @@ def errs(out, ref) -> dict:
 # computes h in FP32, the oracle in float64; where h lies within that difference of a
 # rounding midpoint the two sides pick neighbouring E4M3 codes.  Such a flip moves one
 # element of h by one E4M3 step -- up to 32/448 of its tile's amax with amax / 448 scales
-# and 32/256 with power-of-two scales, and SwiGLU's heavy-tailed h puts a tile's amax 6-8
-# sigma out -- and reaches the output through one column of W_down (elements up to about
-# 4.5 / sqrt(I)): a handful of a row's outputs move by up to 0.1 x 0.143 x 8 = 11 % of the
-# RMS, the Frobenius error barely changes.  A wrong scale, index or tile moves thousands of
-# elements and the Frobenius error with them.  So the FP8 gates are: relative Frobenius
-# <= 5e-3 (the bf16 bound), at most 1e-4 of the elements beyond the bf16 bound (computation
-# error beyond bf16 storage rounding > 2e-2 of the RMS), and every element within 0.15.
+# and 32/256 with power-of-two scales, about 0.4-0.9 sigma of h since SwiGLU's
+# heavy-tailed h puts a tile's amax 6-8 sigma out -- and reaches one output row through a
+# column of W_down (elements ~ N(0, 1/sqrt(I))): some of that row's outputs move by a few
+# per cent of the RMS, up to 0.1 x 0.143 x 8 = 11 % for the largest, while the Frobenius
+# error barely changes.  A wrong scale, index or tile moves a large share of a whole tile
+# (thousands to tens of thousands of elements).  So the FP8 gates are: relative Frobenius
+# <= 5e-3 (the bf16 bound), at most 1e-3 of the elements beyond the bf16 bound
+# (computation error beyond bf16 storage rounding > 2e-2 of the RMS; flips measured
+# 1e-5..1e-4, a 2 % error on one tile of a V3 expert 6e-3), every element within 0.15.
 FP8_TOL_FRO = 5e-3
-FP8_TOL_FRAC = 1e-4
+FP8_TOL_FRAC = 1e-3
 FP8_TOL_MAX = 0.15
 
 

@@ -5,7 +5,7 @@ accumulation) against the oracle's FP8 layer with the same scales.
 
 Codes and scales computed on both sides from the same bf16 inputs match bit for bit.
 Float outputs against the oracle's FP8 layer: the FP8 gates of moe_testutil.fp8_ok
-(relative Frobenius error <= 5e-3, at most 1e-4 of the elements beyond the bf16 bound,
+(relative Frobenius error <= 5e-3, at most 1e-3 of the elements beyond the bf16 bound,
 every element within 0.15 of the RMS -- with power-of-two scales one E4M3 step of h can
 be 32/256 of its tile's amax); against the same layer with x and h left unquantised:
 relative Frobenius error <= 6e-2."""
