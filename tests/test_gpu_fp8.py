@@ -6,7 +6,7 @@ must match bit for bit.  Float outputs are compared with the oracle's FP8 layer
 under the same simulated quantisation with the FP8 gates of moe_testutil.fp8_ok
 (relative Frobenius error <= 5e-3, at most 1e-3 of the elements beyond the bf16
 bound, every element within 0.15 of the RMS: an E4M3 code of h that flips at a
-rounding midpoint moves a handful of a row's outputs, a wrong scale, index or tile
+rounding midpoint moves some of one row's outputs, a wrong scale, index or tile
 moves thousands), and with the same layer left unquantised (x and h exact) at a
 relative Frobenius error <= 6e-2: E4M3's three mantissa bits alone cost about 4.4 %
 there, and the max error against the unquantised layer (20-30 % of the RMS) is

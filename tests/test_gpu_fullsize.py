@@ -14,7 +14,7 @@ once: 2^-9 / sqrt(3) RMS relative error each, about 2e-3 together).
 FP8 (FP32 and power-of-two scales): against the oracle's FP8 layer (same 1x128 /
 128x128 quantisation) the gates of moe_testutil.fp8_ok -- Frobenius <= 5e-3 as bf16,
 at most 1e-3 of the elements beyond the bf16 bound, every element within 0.15 -- since
-an E4M3 code of h that flips at a rounding midpoint moves a handful of a row's outputs
+an E4M3 code of h that flips at a rounding midpoint moves some of one row's outputs
 by up to ~11 % of the RMS (measured: 7.2e-2 on one V3 expert with power-of-two
 scales) while a wrong scale, index or tile moves thousands; against the layer with
 x and h left unquantised the relative Frobenius error must stay below 6e-2 (E4M3's
