@@ -226,14 +226,20 @@ class _View:
         return self.owner.get(int(e), self.which)
 
 
-def _traffic(fp8: bool):
-    """DRAM bytes per launch of the expert-FFN kernels, from the ncu capture recorded in
-    profiles/expert_ffn_traffic.json -- None when the kernel sources changed since."""
+def _traffic(cfg):
+    """DRAM bytes per step of the two expert-GEMM launches at the full V3 shape, from the ncu
+    slice captures recorded in profiles/expert_ffn_traffic.json (scaled to the full launch
+    by its algorithmic bytes) -- None for another shape, or once the kernel sources changed."""
     import hashlib
 
+    if (cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I) not in ((8192, 7168, 256, 1, 8, 2048), (16384, 7168, 256, 1, 8, 2048)):
+        return None
+    if cfg.T != (16384 if cfg.fp8 else 8192):
+        return None
+    key = ("fp8_pow2" if cfg.pow2 else "fp8") if cfg.fp8 else "bf16"
     try:
         with open(os.path.join(ROOT, "profiles", "expert_ffn_traffic.json")) as f:
-            rec = json.load(f)["fp8" if fp8 else "bf16"]
+            rec = json.load(f)[key]
         h = hashlib.sha256()
         for name in rec["sources"]:
             with open(os.path.join(ROOT, "sparse_moe_layer_12_b300", "csrc", name), "rb") as fh:
@@ -685,11 +691,20 @@ def run_ours(args):
     flops = cfg.expert_flops()
     ffn_avg_s = statistics.mean(ffn_ms) / 1e3
     achieved = flops / ffn_avg_s / 1e12
+    # the GEMMs run inside back-to-back steps (tens to hundreds of ms of continuous tensor
+    # work, under the board's power cap): the sustained bf16 figure is their denominator,
+    # the burst figure is reported beside it
+    burst = pk["bf16_tflops"]
     if fp8 and "fp8" in fp8_peaks:
         peak, peak_src = fp8_peaks["fp8"], "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)"
+        burst = peak
+    elif fp8:
+        peak, peak_src = 2.0 * pk["bf16_tflops"], f"{pk_src} bf16 burst x2 (fp8 nominal ratio)"
+        burst = peak
     else:
-        peak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
-        peak_src = f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if fp8 else "")
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        peak_src = (f"{pk_src} bf16 sustained (the FFN runs inside {args.warmup + args.steps}+ back-to-back steps "
+                    "under the power cap; frac_of_burst beside it)")
     # weight bytes the expert GEMMs must stream: every expert that received a token, plus shared
     c_last = state["counts"]
     hit = int((c_last > 0).sum().item()) + cfg.S
@@ -703,8 +718,9 @@ def run_ours(args):
     else:
         roofline = {"bound": "tensor", "kernel": "moe_expert_ffn (grouped gate/up+SwiGLU and down GEMMs)",
                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "frac_of_burst": achieved / burst, "burst_peak": burst,
                     "peak_source": peak_src, "algorithmic_flops": flops,
-                    "traffic": _traffic(fp8) if cfg.name in ("v3", "v3fp8") else None}
+                    "traffic": _traffic(cfg)}
     line = {
         "metric": METRIC,
         "value": world * cfg.T * args.steps / (ms / 1e3),
@@ -722,6 +738,7 @@ def run_ours(args):
         "config": _config_obj(cfg, world),
         "expert_gemm_tflops": achieved,
         "expert_gemm_pct_of_peak": 100.0 * achieved / peak,
+        "expert_gemm_pct_of_burst_peak": 100.0 * achieved / burst,
         "roofline": roofline,
         "stages": _stage_report(cfg, stages, gathers, pk, pk_src),
         "stage_ms": {"expert_ffn": statistics.mean(ffn_ms), "rest": eager_ms / args.steps - statistics.mean(ffn_ms)},
@@ -847,6 +864,7 @@ def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks, name):
            "tokens_per_s": cfg.T * args.steps / (ms / 1e3), "ms_per_step": ms / args.steps,
            "steps": args.steps, "warmup": args.warmup,
            "expert_gemm_tflops": tf, "fp8_peak_tflops": peak, "frac": tf / peak, "peak_source": src,
+           "traffic": _traffic(cfg),
            "stages": _stage_report(cfg, stages, gathers, pk, pk_src), "clocks": ck, "device_status": status}
     del ws, wgu, wd, gs, ds, x
     torch.cuda.empty_cache()
