@@ -745,9 +745,9 @@ def run_ours(args):
         "timing": {"eager_ms_per_step": eager_ms / args.steps,
                    "graph_ms_per_step": None if graph_ms is None else graph_ms / args.steps,
                    "value_from": "graph replay" if ms != eager_ms else "eager launches"},
-        # per step: router, offsets, permute tables, [permuted copy,] schedule, [E4M3 copy of x,]
-        # gate/up, down, combine, bias update
-        "gpu_launches": (8 + (0 if gathers else 1) + (1 if fp8 and (gathers or cfg.S > 0) else 0)) * args.steps,
+        # per step: router (with the load and its offsets), permute tables, [permuted copy,]
+        # schedule, [E4M3 copy of x,] gate/up, down, combine, bias update
+        "gpu_launches": (7 + (0 if gathers else 1) + (1 if fp8 and (gathers or cfg.S > 0) else 0)) * args.steps,
         "dispatch": "rows gathered from x inside the gate/up GEMM" if gathers else "permuted copy + tile loads",
         "clocks": ck,
         "e2e": e2e,

@@ -24,6 +24,9 @@
  *     memory, including the workspace.  The library never allocates or frees.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     none synchronises the host, except moe_get_device_status.
+ *   - A call runs on the calling host thread's current CUDA device, which must
+ *     own the buffers and the stream; in a thread that has not used the CUDA
+ *     runtime yet, the library makes that device's primary context current.
  *   - Arguments are validated before anything is launched; a non-OK status
  *     means nothing was enqueued.  No C++ exception crosses the ABI.
  *   - Row-major tensors must start on a 16-byte boundary.
@@ -98,9 +101,11 @@ typedef struct CUstream_st* moe_stream_t;
 
 /* Bytes of workspace every call below needs for `shape` (the maximum over all
  * calls, so one buffer serves them all); 0 if the shape is invalid.  The
- * workspace must start on 256 bytes and its first 256 bytes (the device
- * status word) must be zero before its first use; the rest needs no
- * initialisation. */
+ * workspace must start on 256 bytes and its first 2048 bytes (the control
+ * block: the device status word, and the router's load counters, which every
+ * moe_route call leaves cleared) must be zero before its first use; the rest
+ * needs no initialisation.  Calls that share a workspace run in stream order
+ * (not concurrently). */
 MOE_API size_t moe_workspace_bytes(const moe_shape_t* shape);
 
 /* Router ("deepseek-v3-report", load-balancing paragraph; "DeepSeek-V3 详解"
@@ -117,7 +122,9 @@ MOE_API size_t moe_workspace_bytes(const moe_shape_t* shape);
  *   counts       int32 [E]     out    tokens routed to each expert (load)
  *   offsets      int32 [E+1]   out    exclusive prefix sum of counts
  * z is accumulated in FP32 on the tensor cores; s, s + b and the gates are
- * FP32.  Deterministic run to run. */
+ * FP32.  Deterministic run to run.  One kernel launch (T > 0): the load is
+ * summed in the workspace's control block and written out, with its prefix
+ * sum, by the last block to finish. */
 MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const void* w_router,
                        const float* bias, const float* logit_offset, int32_t* topk_idx,
                        float* topk_gate, int32_t* counts, int32_t* offsets, void* ws,

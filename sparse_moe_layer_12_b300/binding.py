@@ -69,6 +69,9 @@ _SIGS = {
 
 _lib = None
 
+# bytes at the start of a forward workspace that must be zero before its first use
+WS_CTRL_BYTES = 2048
+
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load libmoe.so (raises if it has not been built)."""
@@ -137,7 +140,7 @@ def alloc_workspace(shape: Shape, device="cuda") -> torch.Tensor:
     if n == 0:
         raise ValueError("invalid shape")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
-    ws[:256].zero_()  # the device status word starts clear
+    ws[:WS_CTRL_BYTES].zero_()  # the control block (status word, router load counters) starts clear
     return ws
 
 

@@ -56,7 +56,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   const bool f8 = is_fp8(s.dtype);
   const size_t es = f8 ? 1 : 2;
   size_t o = 0;
-  L.status = o;      o = align_up(o + 256, A);
+  L.status = o;      o = align_up(o + kWsCtrlBytes, A);
   L.counts = o;      o = align_up(o + 4 * (size_t)s.E, A);
   L.offsets = o;     o = align_up(o + 4 * ((size_t)s.E + 1), A);
   L.idx = o;         o = align_up(o + 4 * Tk, A);
@@ -174,7 +174,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The tensor-map encoder is a driver entry point that needs the calling thread's
+// context to be current, which the runtime only makes so on its first call in that
+// thread: a host thread whose first library call builds a tensor map gets the
+// current device's primary context here, once.
+static bool thread_context_ready() {
+  thread_local bool ready = false;
+  if (!ready) ready = cudaFree(nullptr) == cudaSuccess;
+  return ready;
+}
+
 static EncodeTiledFn encode_fn() {
+  if (!thread_context_ready()) return nullptr;
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {

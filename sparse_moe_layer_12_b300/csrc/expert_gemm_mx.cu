@@ -388,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float amax =
                 fmaxf(fmaxf(gmax[lane], gmax[32 + lane]), fmaxf(gmax[64 + lane], gmax[96 + lane]));
             const float sc = pow2_scale(amax);
-            gmax[lane] = sc;
+            gmax[lane] = pow2_recip(sc);  // the codes below are h * (1 / sc) = h / sc exactly
             if (lane < rows_here && fb0 < I) {
               const int row = ti.out_row0 + c0 + lane;
               out_scale[(size_t)row * (I / 128) + fb0 / 128] = sc;
@@ -400,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* sb = reinterpret_cast<uint8_t*>(sg);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const uint16_t c2 = f32x2_to_e4m3x2(__fdiv_rn(h[i], gmax[i]), __fdiv_rn(h[i + 1], gmax[i + 1]));
+            const uint16_t c2 = f32x2_to_e4m3x2(__fmul_rn(h[i], gmax[i]), __fmul_rn(h[i + 1], gmax[i + 1]));
             sb[i * 128 + f] = static_cast<uint8_t>(c2 & 0xff);
             sb[(i + 1) * 128 + f] = static_cast<uint8_t>(c2 >> 8);
           }

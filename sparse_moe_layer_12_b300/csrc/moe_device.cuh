@@ -488,6 +488,15 @@ __device__ __forceinline__ float pow2_scale(float amax) {
   return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
+// 1 / scale, exactly, for a scale from pow2_scale (2^-127 .. 2^127).  For a power of
+// two, v * (1 / scale) and v / scale are the same real number rounded the same way, so
+// the product gives the quotient's bits without a division.
+__device__ __forceinline__ float pow2_recip(float scale) {
+  const int be = static_cast<int>((__float_as_uint(scale) >> 23) & 0xFFu);  // 0 for 2^-127
+  const int r = be == 0 ? 127 : 127 - be;                                      // exponent of 1 / scale
+  return r >= -126 ? __uint_as_float(static_cast<uint32_t>(r + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
 // UE8M0 byte of a power-of-two FP32 scale: its biased exponent (2^-127, the one
 // subnormal scale, has exponent field 0 = UE8M0 2^-127 as well).
 __device__ __forceinline__ uint32_t ue8m0_of(float pow2) { return (__float_as_uint(pow2) >> 23) & 0xFFu; }
@@ -505,8 +514,14 @@ __device__ __forceinline__ float quant_tile16(const float (&f)[8], uint2& q) {
   for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = POW2 ? pow2_scale(amax) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
   uint32_t c[4];
+  if (POW2) {
+    const float inv = pow2_recip(scale);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+    for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = f32x2_to_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+  }
   q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   return scale;
 }

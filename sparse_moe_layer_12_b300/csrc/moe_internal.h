@@ -84,8 +84,13 @@ WsLayout ws_layout(const moe_shape_t& s);
 // h and its scales), packed; the other fields are 0 and unused.  `total` is its size.
 WsLayout ffn_ws_layout(const moe_shape_t& s);
 
-// status word helpers (the word lives at offset 0 of the workspace)
+// The workspace's control block (its first kWsCtrlBytes, zero before first use): the
+// device status word at offset 0, and at offset 256 the router's load counters
+// (kMaxE counts and a ticket), which every router launch leaves cleared.
+constexpr size_t kWsCtrlBytes = 2048;
 inline int* ws_status(void* ws) { return reinterpret_cast<int*>(ws); }
+inline int* ws_load_acc(void* ws) { return reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + 256); }
+static_assert(256 + 4 * (kMaxE + 1) <= kWsCtrlBytes, "router load counters do not fit the control block");
 
 // host helpers
 moe_status_t check_ws(const moe_shape_t& s, void* ws, size_t ws_bytes);

@@ -17,7 +17,9 @@
 // tokens and receives the other CTA's partial logits for them in one bulk
 // shared-to-shared copy.  Warp roles: warp 0 TMA producer, warp 1 MMA issuer (even
 // CTA), warps 2-5 move TMEM to shared memory (one lane quadrant each); then all 16
-// warps select the top-k of whole tokens (8 experts a lane).
+// warps select the top-k of whole tokens (8 threads a token).  The load histogram
+// goes into counters in the workspace; the last CTA to finish writes counts and
+// offsets and clears the counters, so one launch does the whole call.
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -51,6 +53,11 @@ __host__ __device__ inline RouterSmem router_smem(int E, int ksplit) {
 }
 
 constexpr size_t kCtrlBytes = 4096;  // barriers, flags, bias, offsets, histogram
+
+// The candidate filter of the top-k: scores are first estimated as
+// v' = (1 + tanh(z' / 2)) / 2 + b with one tanh.approx (relative error below 2^-10.9,
+// so |v' - v| < 2.5e-4 plus rounding); kFilterEps bounds |v' - v| with margin.
+constexpr float kFilterEps = 2.0e-3f;
 
 __device__ __forceinline__ uint32_t order_key(float v) {  // monotone float -> uint32
   const uint32_t b = __float_as_uint(v);
@@ -154,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, int T,
                   int d, int E, int k, const float* __restrict__ bias, const float* __restrict__ logit_offset,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int32_t* __restrict__ counts,
-                  int ksplit, int n_group, int topk_group, int* __restrict__ status) {
+                  int32_t* __restrict__ offsets, int* __restrict__ load_acc, int ksplit, int n_group, int topk_group,
+                  int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const RouterSmem L = router_smem(E, ksplit);
@@ -168,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 132);
   volatile int* zero_flag = reinterpret_cast<volatile int*>(ctrl + 136);  // stays 0
   int* last_round = reinterpret_cast<int*>(ctrl + 144);                   // [kStages]
+  int* s_last = reinterpret_cast<int*>(ctrl + 200);                       // this CTA finished last
   float* s_bias = reinterpret_cast<float*>(ctrl + 256);
   float* s_off = s_bias + kMaxE;
   int* s_hist = reinterpret_cast<int*>(s_off + kMaxE);
+  int* s_wsum = s_hist;  // [kThreads / 32] warp sums of the offsets scan, once s_hist is spent
   float* s_z = reinterpret_cast<float*>(smem);                      // [128][np + 1], after the MMAs
   float* s_recv = reinterpret_cast<float*>(smem + L.z_bytes);       // [64][np + 1], K split only
 
@@ -292,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kRouterTileM / 2 / 16; ++c)
         bulk_copy_to_peer(dst + c * chunk, s_z + (size_t)(give + 16 * c) * (np + 1), chunk, bar);
     }
-    if (mbar_wait(xchg, 0, abort_flag, status, status + 1, kSiteRouterEpi)) {
+    // the partner's partial is added in place here for the warp-per-token path, and as
+    // it is read by the 8-threads-per-token path below
+    if (mbar_wait(xchg, 0, abort_flag, status, status + 1, kSiteRouterEpi) && (n_group > 0 || k > 8)) {
       for (int row = row_lo + warp; row < row_hi; row += kThreads / 32) {
         float* zz = s_z + row * (np + 1);
         const float* pp = s_recv + (row - row_lo) * (np + 1);
@@ -302,18 +314,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
   if (!*abort_flag && n_group == 0 && k <= 8) {
-    // ---- phase 2, plain top-k (k <= 8): 8 threads per token.  Thread (token tl, sub)
-    // scores experts e = 32 b + 4 sub + c (b = 0..7, c = 0..3) -- ascending in its own
-    // order, and for a fixed step the 32 lanes of a warp (4 tokens x 8 subs) hit 32
-    // different shared-memory banks -- keeping its best 8 by insertion (a later expert
-    // enters only on a strictly larger score, so ties keep the lower index); the 8
-    // lists of a token are then merged.  gates = chosen s / sum of chosen s (sum in
-    // ranking order).
+    // ---- phase 2, plain top-k (k <= 8): 8 threads per token.  Thread (token, sub) owns
+    // experts e = 32 b + 4 sub + c (b = 0..7, c = 0..3): for a fixed step the 32 lanes
+    // of a warp (4 tokens x 8 subs) read 32 different shared-memory banks.
+    //  (1) estimates v' of its 32 scores (kFilterEps above) and their maximum; tau' =
+    //      the smallest of the token's 8 maxima.  Every thread's best element has
+    //      v >= tau' - eps, so at least 8 scores reach tau' - eps, and each that does
+    //      has v' >= tau' - 2 eps: those candidates hold the token's top-k;
+    //  (2) the exact score v = sigmoid(z) + b of each candidate enters the thread's
+    //      descending list of 8, experts in ascending order (a later expert enters only
+    //      on a strictly larger score, so ties keep the lower index);
+    //  (3) the 8 lists of the token are merged; gates = chosen s / sum of the chosen s,
+    //      summed in ranking order.
     const int sub = threadIdx.x & 7;
     for (int tb = row_lo; tb < row_hi; tb += kThreads / 8) {
       const int row = tb + (threadIdx.x >> 3);
       const bool live = row < row_hi && tok0 + row < T;
-      const float* zr = s_z + row * (np + 1);
+      float* zr = s_z + row * (np + 1);
+      const float* pr = s_recv + (row - row_lo) * (np + 1);  // the partner's partial (K split)
+      auto logit = [&](int e) -> float {
+        float z = zr[e];
+        if (ksplit == 2) z = z + pr[e];
+        return z + s_off[e];
+      };
+      auto score = [&](int e) -> float {
+        const float sc = __fdividef(1.0f, 1.0f + __expf(-logit(e)));
+        const float b = sc + s_bias[e];
+        return (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
+      };
+      float v[32];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = 32 * (j >> 2) + 4 * sub + (j & 3);
+        float a = -INFINITY;
+        if (live && e < E) {
+          float t;
+          asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * logit(e)));
+          a = fminf(fmaxf(fmaf(0.5f, t, 0.5f) + s_bias[e], -3.0e38f), 3.0e38f);  // NaN -> -3e38
+        }
+        v[j] = a;
+        mx = fmaxf(mx, a);
+      }
+      float tau = mx;
+      tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 1));
+      tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 2));
+      tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 4));
+      tau -= 2.0f * kFilterEps;
+      uint32_t cand = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) cand |= (v[j] < tau ? 0u : 1u) << j;
+      if (!live) cand = 0;
       float lv[8];
       int le[8];
 #pragma unroll
@@ -321,45 +372,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         lv[i] = -INFINITY;
         le[i] = 0x7fffffff;
       }
-#pragma unroll 4
-      for (int j = 0; j < 32; ++j) {
+      while (cand) {
+        const int j = __ffs(cand) - 1;
+        cand &= cand - 1;
         const int e = 32 * (j >> 2) + 4 * sub + (j & 3);
-        float v = -INFINITY;
-        if (live && e < E) {
-          const float z = zr[e] + s_off[e];
-          const float sc = __fdividef(1.0f, 1.0f + __expf(-z));
-          const float b = sc + s_bias[e];
-          v = (b == b) ? fminf(fmaxf(b, -3.0e38f), 3.0e38f) : -3.0e38f;
-        }
+        const float w = e < E ? score(e) : -INFINITY;
         bool c[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = v > lv[i];
+        for (int i = 0; i < 8; ++i) c[i] = w > lv[i];
 #pragma unroll
         for (int i = 7; i >= 1; --i) {
-          lv[i] = c[i - 1] ? lv[i - 1] : (c[i] ? v : lv[i]);
+          lv[i] = c[i - 1] ? lv[i - 1] : (c[i] ? w : lv[i]);
           le[i] = c[i - 1] ? le[i - 1] : (c[i] ? e : le[i]);
         }
-        lv[0] = c[0] ? v : lv[0];
+        lv[0] = c[0] ? w : lv[0];
         le[0] = c[0] ? e : le[0];
       }
       merge_top8(lv, le);
-      // affinities of the chosen experts (recomputed from z, as above) and their sum
-      float sc_sel[8], sum = 0.0f;
+      // lane `sub` of the token's group takes rank sub; the k affinities are gathered
+      // from the group's lanes and summed in ranking order
+      int my_e = le[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) my_e = sub == i ? le[i] : my_e;
+      float my_s = 0.0f;
+      if (live && sub < k && my_e < E) my_s = __fdividef(1.0f, 1.0f + __expf(-logit(my_e)));
+      float sum = 0.0f;
+      const int grp = lane & ~7;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int e = le[i];
-        sc_sel[i] = 0.0f;
-        if (live && i < k && e < E) sc_sel[i] = __fdividef(1.0f, 1.0f + __expf(-(zr[e] + s_off[e])));
-        if (i < k) sum += sc_sel[i];
+        const float si = __shfl_sync(0xffffffffu, my_s, grp | i);
+        if (i < k) sum += si;
       }
       if (live && sub < k) {
-        int my_e = le[0];
-        float my_s = sc_sel[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) {
-          my_e = sub == i ? le[i] : my_e;
-          my_s = sub == i ? sc_sel[i] : my_s;
-        }
         const int t = tok0 + row;
         topk_idx[(size_t)t * k + sub] = my_e;
         topk_gate[(size_t)t * k + sub] = __fdiv_rn(my_s, sum);
@@ -449,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads)
-    if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
+    if (s_hist[e]) atomicAdd(&load_acc[e], s_hist[e]);
   __syncthreads();
   if (warp == 0 && lane == 0 && *abort_flag && q == 0) {
     // this pair's loads completed on this CTA's barriers: do not leave TMA writes in flight
@@ -465,24 +509,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, ncols);
   }
-}
-
-// offsets[0] = 0, offsets[i+1] = offsets[i] + counts[i]
-__global__ void offsets_kernel(const int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int E) {
-  __shared__ int buf[2][kMaxE];
-  const int i = threadIdx.x;
-  int v = i < E ? counts[i] : 0;
-  int cur = 0;
-  buf[0][i] = v;
+  // ---- the load: every CTA has added its histogram into load_acc[0, E); a ticket in
+  // load_acc[kMaxE] finds the last CTA, which writes counts and their exclusive prefix
+  // sum (offsets[0] = 0, offsets[i+1] = offsets[i] + counts[i]) and clears the counters
+  // and the ticket for the next call
+  __threadfence();
   __syncthreads();
-  for (int off = 1; off < kMaxE; off <<= 1) {
-    const int nv = buf[cur][i] + (i >= off ? buf[cur][i - off] : 0);
-    buf[cur ^ 1][i] = nv;
-    cur ^= 1;
+  if (threadIdx.x == 0) *s_last = atomicAdd(&load_acc[kMaxE], 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    const int c = threadIdx.x < E ? atomicExch(&load_acc[threadIdx.x], 0) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
     __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_wsum[w];
+    if (threadIdx.x < E) {
+      counts[threadIdx.x] = c;
+      offsets[threadIdx.x + 1] = base + incl;
+    }
+    if (threadIdx.x == 0) {
+      offsets[0] = 0;
+      atomicExch(&load_acc[kMaxE], 0);
+    }
   }
-  if (i < E) offsets[i + 1] = buf[cur][i];
-  if (i == 0) offsets[0] = 0;
 }
 
 }  // namespace
@@ -490,8 +546,12 @@ __global__ void offsets_kernel(const int32_t* __restrict__ counts, int32_t* __re
 moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_router, const float* bias,
                           const float* logit_offset, int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
                           void* ws, cudaStream_t st) {
-  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (s.T > 0) {
+  if (s.T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (s.E + 1), st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  {
     const int nsuper = (s.T + 2 * kRouterTileM - 1) / (2 * kRouterTileM);  // 256-token tiles
     CUtensorMap mx, mw;
     const int np = (s.E + 15) & ~15;
@@ -522,13 +582,12 @@ moe_status_t launch_route(const moe_shape_t& s, const void* x, const void* w_rou
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, ksplit,
-                           s.n_group, s.topk_group, status) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, mx, mw, s.T, s.d, s.E, s.k, bias, logit_offset, idx, gate, counts, offsets,
+                           ws_load_acc(ws), ksplit, s.n_group, s.topk_group, status) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  offsets_kernel<<<1, kMaxE, 0, st>>>(counts, offsets, s.E);
-  return cuda_status(cudaGetLastError());
+  return MOE_OK;
 }
 
 }  // namespace moe
