@@ -40,7 +40,9 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kChunk = kChunkMxMax;           // tokens per tile (N)
-constexpr int kThreads = 320;                 // producer warp, MMA warp, 8 epilogue warps
+constexpr int kProducers = 2;                 // producer warps: 0 and 10 .. 8 + kProducers (4 measured slower)
+constexpr int kThreads = 32 * (9 + kProducers);  // + MMA warp 1 and epilogue warps 2-9
+static_assert(kStages % kProducers == 0, "a producer warp owns whole operand stages");
 constexpr int kKStagger = 5;                  // K-block offset between consecutive feature blocks
 constexpr uint32_t kATile = 128 * 128;        // 128 weight rows x 128 K bytes
 constexpr uint32_t kBTile = 128 * 128;        // this CTA's half of <= 224 token rows: one 128-row box
@@ -188,11 +190,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t full_leader = map_to_rank(smem_u32(full), 0);
   const uint32_t tmem_empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
 
-  if (warp == 0) {
-    // ---------------- producer warp: lane 0 issues the TMA loads of this CTA's 2 x 128
-    // weight rows and half of the token rows; every lane writes its line of the stage's
-    // scale tile (token scales read two K blocks ahead)
-    uint32_t it = 0;
+  if (warp == 0 || warp >= 10) {
+    // ---------------- producer warps: producer p (warp 0, then warps 10, 11, ...) fills the
+    // operand stages s with s % kProducers = p, i.e. the K blocks whose running count is p
+    // modulo kProducers; lane 0 issues the TMA loads of this CTA's 2 x 128 weight rows and
+    // half of the token rows, every lane writes its line of the stage's scale tile.  Each
+    // warp reads the scales of its own K blocks two of them ahead.
+    const uint32_t pw = warp == 0 ? 0u : static_cast<uint32_t>(warp - 9);
+    uint32_t it = 0;  // running K-block count over the tiles (both warps count every block)
     bool ok = true;
     GroupCursor cur;
     for (int tile = pair; tile < total && ok; tile += npairs) {
@@ -232,8 +237,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) tv[j] = live[j] ? static_cast<uint32_t>(__ldg(sb + (size_t)kq * plane + trow[j])) : 127u;
       };
       // one K block: wait for the stage, write this lane's line of its scale tile, issue the loads
-      auto stage = [&](int kb, float w0v, float w1v, const uint32_t (&tv)[8]) -> bool {
-        const int s = it % kStages, r = it / kStages;
+      auto stage = [&](int kb, uint32_t itk, float w0v, float w1v, const uint32_t (&tv)[8]) -> bool {
+        const int s = itk % kStages, r = itk / kStages;
         int waited = 1;
         if (lane == 0)
           waited = mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status, status + 1, kSiteGemmProducer) ? 1 : 0;
@@ -268,20 +273,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d_pair(st + 2 * kATile, mb, fb, kq * 128, brow);
           last_round[s] = r;
         }
-        ++it;
         return true;
       };
-      load_scales(0, ew0, ew1, et);
-      if (nk > 1) load_scales(1, ow0, ow1, ot);
-      for (int kb = 0; kb < nk && ok; kb += 2) {
-        ok = stage(kb, ew0, ew1, et);
+      // this warp's K blocks of the tile: kb0, kb0 + P, kb0 + 2P, ... (P = kProducers);
+      // register set E takes kb0 + 2jP, set O kb0 + (2j + 1)P
+      constexpr int P = kProducers;
+      const int kb0 = static_cast<int>((pw + P - it % P) % P);
+      if (kb0 < nk) load_scales(kb0, ew0, ew1, et);
+      if (kb0 + P < nk) load_scales(kb0 + P, ow0, ow1, ot);
+      for (int kb = kb0; kb < nk && ok; kb += 2 * P) {
+        ok = stage(kb, it + kb, ew0, ew1, et);
         if (!ok) break;
-        if (kb + 2 < nk) load_scales(kb + 2, ew0, ew1, et);
-        if (kb + 1 < nk) {
-          ok = stage(kb + 1, ow0, ow1, ot);
-          if (ok && kb + 3 < nk) load_scales(kb + 3, ow0, ow1, ot);
+        if (kb + 2 * P < nk) load_scales(kb + 2 * P, ew0, ew1, et);
+        if (kb + P < nk) {
+          ok = stage(kb + P, it + kb + P, ow0, ow1, ot);
+          if (ok && kb + 3 * P < nk) load_scales(kb + 3 * P, ow0, ow1, ot);
         }
       }
+      it += nk;
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
