@@ -57,6 +57,9 @@ def _args():
     p.add_argument("--set", default="", help="override workload fields, e.g. T=512,E=16 (profiling slices)")
     p.add_argument("--only", default="", choices=["", "route", "backward"],
                    help="time one stage alone: the router, or the layer's backward pass")
+    p.add_argument("--parallel", default="dp", choices=["dp", "ep"],
+                   help="dp: every rank holds all experts (the default line); ep: the routed experts split "
+                        "over the ranks, rows exchanged by all-to-all")
     return p.parse_args()
 
 
@@ -871,10 +874,82 @@ def _fp8_run(B, dp, I, dev, args, stream, pk, pk_src, fp8_peaks, name):
     return res
 
 
+def run_ep(args):
+    """The expert-parallel layer (sparse_moe_layer_12_b300/ep.py): each of the N ranks routes its
+    own T tokens, holds E/N routed experts and a replica of the router and the shared expert;
+    rows travel by all-to-all (NCCL between GPUs; with one rank the exchange is a local copy)."""
+    import torch
+    import torch.distributed as dist
+
+    from sparse_moe_layer_12_b300 import binding as B
+    from sparse_moe_layer_12_b300 import ep
+    from sparse_moe_layer_12_b300 import inputs as I
+
+    world, rank, local = _setup_dist()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    cfg = _config(args)
+    B.load()
+    lo, hi = ep.expert_range(cfg.E, world, rank)
+    x = I.make_x(cfg.with_(seed=cfg.seed + rank), dev)
+    wr, bias = I.make_router(cfg, dev), I.make_bias(cfg, dev)
+    sc = None
+    if cfg.fp8:
+        wgu, gs, wd, ds = I.make_experts_fp8(cfg, dev, pow2=cfg.pow2)
+        sc = dict(gate_up_local=gs[lo:hi].contiguous(), down_local=ds[lo:hi].contiguous(),
+                  gate_up_shared=gs[cfg.E:].contiguous(), down_shared=ds[cfg.E:].contiguous())
+    else:
+        wgu, wd = I.make_experts(cfg, dev)
+    w_loc = (wgu[lo:hi].contiguous(), wd[lo:hi].contiguous())
+    w_sh = (wgu[cfg.E:].contiguous(), wd[cfg.E:].contiguous())
+    del wgu, wd
+    torch.cuda.empty_cache()
+    ops = ep.CudaOps(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, world, wr, w_loc[0], w_loc[1], w_sh[0], w_sh[1],
+                     fp8=cfg.fp8, scales=sc, n_group=cfg.n_group, topk_group=cfg.topk_group, pow2=cfg.pow2)
+    tp = ep.DistTransport() if world > 1 else ep.LocalTransport(1).view(0)
+    er = ep.EPRank(ops, tp, cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, rank, world)
+    off = I.make_logit_offset(cfg, dev)
+    for _ in range(args.warmup):
+        er.forward(x, bias, off, update_bias=True, gamma=cfg.gamma)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks()
+    clocks.start()
+    a.record(stream)
+    for _ in range(args.steps):
+        er.forward(x, bias, off, update_bias=True, gamma=cfg.gamma)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    status = ops.device_status()
+    if rank == 0:
+        line = {"metric": METRIC, "value": world * cfg.T * args.steps / (ms / 1e3), "unit": "tokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": ("fp8-e4m3 (fp32 acc)" if cfg.fp8 else "bf16 (fp32 acc)"),
+                "data": "synthetic (seeded, random-init weights of the layer's shape)",
+                "config": {**_config_obj(cfg, world), "parallelism": f"ep{world} (routed experts split over the ranks)"},
+                "clocks": ck, "device_status": status,
+                "note": "each step synchronises the host once (the all-to-all split sizes)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.parallel == "ep":
+        run_ep(args)
     elif args.only == "route":
         run_route_only(args)
     elif args.only == "backward":

@@ -40,6 +40,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kChunk = kChunkMxMax;           // tokens per tile (N)
+constexpr int kMine = kChunk / 64;            // 32-column chunks per epilogue group, at most
 constexpr int kProducers = 2;                 // producer warps: 0 and 10 .. 8 + kProducers (4 measured slower)
 constexpr int kThreads = 32 * (9 + kProducers);  // + MMA warp 1 and epilogue warps 2-9
 static_assert(kStages % kProducers == 0, "a producer warp owns whole operand stages");
@@ -361,33 +362,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nm = (ti.n + 15) & ~15;
       const int nchunk = (nm + 31) / 32;
       const int mine = nchunk > grp ? (nchunk - grp + 1) / 2 : 0;
-      if (mine == 0) {
-        tc_fence_before();
-        mbar_arrive_remote(tmem_empty_leader);
-      }
-      for (int ci = 0; ci < mine; ++ci) {
-        const int c0 = (grp + 2 * ci) * 32;
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tmem + lane_base + c0, ra);
-        tmem_ld32(tmem + lane_base + kAcc1 + c0, rb);
-        tmem_ld_wait();
-        if (ci == mine - 1) {  // this group is done with TMEM for this tile
-          tc_fence_before();
-          mbar_arrive_remote(tmem_empty_leader);
+      // (a) every column chunk of this group out of TMEM into registers -- gate/up: h =
+      // silu(g) * u in FP32; down: y as bf16 pairs, channel block 0 then 1 -- and TMEM
+      // released, so that the next tile's MMAs run under (b)
+      uint32_t keep[kMine][32];
+#pragma unroll
+      for (int ci = 0; ci < kMine; ++ci) {
+        if (ci < mine) {
+          const int c0 = (grp + 2 * ci) * 32;
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tmem + lane_base + c0, ra);
+          tmem_ld32(tmem + lane_base + kAcc1 + c0, rb);
+          tmem_ld_wait();
+          if (MODE == kGateUp) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(ra[i]);
+              keep[ci][i] = __float_as_uint(__fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(rb[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              keep[ci][i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+              keep[ci][16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+            }
+          }
         }
+      }
+      tc_fence_before();
+      mbar_arrive_remote(tmem_empty_leader);  // this group is done with TMEM for this tile
+      // (b) per chunk: quantise h (one 1x128 tile per token: this CTA's 128 features) or
+      // convert y, transposed through the staging tile into whole-row stores
+#pragma unroll
+      for (int ci = 0; ci < kMine; ++ci) {
+        if (ci >= mine) continue;
+        const int c0 = (grp + 2 * ci) * 32;
         const int rows_here = min(32, ti.n - c0);
         if (MODE == kGateUp) {
-          // h = silu(g) * u for feature f, tokens c0 .. c0 + 31; one 1x128 tile per token
-          float h[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float g = __uint_as_float(ra[i]);
-            h[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(rb[i]);
-          }
           uint32_t mx = 0;  // |h| max over this warp's 32 features, token column = lane
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[i])));
+            const uint32_t m = __reduce_max_sync(0xffffffffu, keep[ci][i] & 0x7fffffffu);
             if (lane == i) mx = m;
           }
           gmax[q * 32 + lane] = __uint_as_float(mx);
@@ -409,7 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* sb = reinterpret_cast<uint8_t*>(sg);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const uint16_t c2 = f32x2_to_e4m3x2(__fmul_rn(h[i], gmax[i]), __fmul_rn(h[i + 1], gmax[i + 1]));
+            const uint16_t c2 = f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(keep[ci][i]), gmax[i]),
+                                                __fmul_rn(__uint_as_float(keep[ci][i + 1]), gmax[i + 1]));
             sb[i * 128 + f] = static_cast<uint8_t>(c2 & 0xff);
             sb[(i + 1) * 128 + f] = static_cast<uint8_t>(c2 >> 8);
           }
@@ -428,8 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              sg[i * kStgStride + f] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(pass == 0 ? ra[i] : rb[i])));
+              sg[i * kStgStride + f] = static_cast<uint16_t>(keep[ci][pass * 16 + i / 2] >> (16 * (i & 1)));
             named_bar_sync(1 + grp, 128);
             const int ch = etid & 15;
             const int col = ti.mp * 512 + pass * 256 + static_cast<int>(rank) * 128 + ch * 8;

@@ -17,7 +17,9 @@ constexpr int kMaxS = 8;
 constexpr int kMaxK = 16;
 constexpr int kRouterTileM = 128;  // tokens per router tile
 constexpr int kChunkMax = 256;     // tokens per expert-GEMM tile (tcgen05 N)
-constexpr int kChunkMxMax = 224;   // tokens per tile of the block-scaled FP8 GEMM (TMEM also holds scales)
+// tokens per tile of the block-scaled FP8 GEMM: each of its two epilogue groups holds its
+// (at most three) 32-token chunks in registers between reading and releasing TMEM
+constexpr int kChunkMxMax = 192;
 constexpr int kBoxRows = 32;       // token rows per TMA box in the expert GEMM
 constexpr size_t kForwardGatherMaxRows = 4096;  // moe_forward gathers routed rows while T*k <= this
 

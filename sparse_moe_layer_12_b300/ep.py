@@ -172,11 +172,11 @@ class CudaOps:
     w_gate_up_shared [S, 2I, d] / w_down_shared [S, d, I] likewise."""
 
     def __init__(self, T, d, E, S, k, I, world, w_router, w_gate_up_local, w_down_local, w_gate_up_shared,
-                 w_down_shared, fp8=False, scales=None, n_group=0, topk_group=0):
+                 w_down_shared, fp8=False, scales=None, n_group=0, topk_group=0, pow2=False):
         from sparse_moe_layer_12_b300 import binding as B
 
         self.B = B
-        self.T, self.d, self.E, self.S, self.k, self.I, self.fp8 = T, d, E, S, k, I, fp8
+        self.T, self.d, self.E, self.S, self.k, self.I, self.fp8, self.pow2 = T, d, E, S, k, I, fp8, pow2
         self.E_loc = E // world
         self.wr = w_router
         self.wgu, self.wd = w_gate_up_local, w_down_local
@@ -184,8 +184,9 @@ class CudaOps:
         sc = scales or {}
         self.gs, self.ds = sc.get("gate_up_local"), sc.get("down_local")
         self.gs_sh, self.ds_sh = sc.get("gate_up_shared"), sc.get("down_shared")
-        self.shape = B.make_shape(T, d, E, S, k, I, fp8, n_group, topk_group)
-        self.shape_sh = B.make_shape(T, d, 1, 0, 1, I, fp8)  # one shared expert as a dense one-expert layer
+        self.shape = B.make_shape(T, d, E, S, k, I, fp8, n_group, topk_group, pow2=pow2)
+        # one shared expert as a dense one-expert layer
+        self.shape_sh = B.make_shape(T, d, 1, 0, 1, I, fp8, pow2=pow2)
         self.ws = B.alloc_workspace(self.shape, w_router.device)
         self.ws_sh = B.alloc_workspace(self.shape_sh, w_router.device)
         self._ws_loc = None
@@ -205,7 +206,7 @@ class CudaOps:
     def local_ffn(self, x_loc, xs_loc, loc_off):
         R = x_loc.shape[0]
         B = self.B
-        shape = B.make_shape(R, self.d, self.E_loc, 0, 1, self.I, self.fp8)
+        shape = B.make_shape(R, self.d, self.E_loc, 0, 1, self.I, self.fp8, pow2=self.pow2)
         need = B.workspace_bytes(shape)
         if self._ws_loc is None or self._ws_loc.numel() < need:
             self._ws_loc = B.alloc_workspace(shape, x_loc.device)
@@ -229,8 +230,8 @@ class CudaOps:
 
     def bias_update(self, counts, bias, T_global, gamma):
         B = self.B
-        B.moe_bias_update(B.make_shape(T_global, self.d, self.E, self.S, self.k, self.I, self.fp8), counts, bias,
-                          gamma)
+        B.moe_bias_update(B.make_shape(T_global, self.d, self.E, self.S, self.k, self.I, self.fp8, pow2=self.pow2),
+                          counts, bias, gamma)
 
     def device_status(self) -> int:
         """The first non-OK device status of this rank's workspaces (read and cleared)."""

@@ -77,12 +77,12 @@ def test_regroup_rejects_inconsistent_counts(libmoe):
     assert B.moe_get_device_status(ws) == 7
 
 
-def _ep_layer(cfg, G, fp8=False):
+def _ep_layer(cfg, G, fp8=False, pow2=False):
     """Per-rank tokens, the layer's weights split over G ranks, and G CudaOps."""
     wr = I.make_router(cfg, DEV)
     bias = I.make_bias(cfg, DEV)
     if fp8:
-        wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV)
+        wgu, gs, wd, ds = I.make_experts_fp8(cfg, DEV, pow2=pow2)
     else:
         (wgu, wd), gs, ds = I.make_experts(cfg, DEV), None, None
     xs = [I.make_x(cfg.with_(seed=cfg.seed + 100 * r), DEV) for r in range(G)]
@@ -94,7 +94,7 @@ def _ep_layer(cfg, G, fp8=False):
             sc = dict(gate_up_local=gs[lo:hi], down_local=ds[lo:hi], gate_up_shared=gs[cfg.E:],
                       down_shared=ds[cfg.E:])
         ops.append(ep.CudaOps(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, G, wr, wgu[lo:hi], wd[lo:hi], wgu[cfg.E:],
-                              wd[cfg.E:], fp8=fp8, scales=sc))
+                              wd[cfg.E:], fp8=fp8, scales=sc, pow2=pow2))
     return wr, bias, wgu, wd, gs, ds, xs, ops
 
 
@@ -151,18 +151,19 @@ def test_ep_layer_matches_forward(libmoe, name, G, T):
         np.testing.assert_array_equal(biases[r].cpu().numpy(), want_b)
 
 
-def test_ep_layer_fp8(libmoe):
+@pytest.mark.parametrize("pow2", [False, True])
+def test_ep_layer_fp8(libmoe, pow2):
     cfg = I.CONFIGS["tiny"]
     G = 2
-    wr, bias, wgu, wd, gs, ds, xs, ops = _ep_layer(cfg, G, fp8=True)
+    wr, bias, wgu, wd, gs, ds, xs, ops = _ep_layer(cfg, G, fp8=True, pow2=pow2)
     res, _ = _run_ep(cfg, G, ops, xs, bias)
-    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8=True)
+    s = B.make_shape(cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I, fp8=True, pow2=pow2)
     for r in range(G):
         assert ops[r].device_status() == 0
         out = res[r][0]
         ref_out, *_ = B.moe_forward(s, xs[r], wr, bias.clone(), wgu, wd, w_gu_scale=gs, w_down_scale=ds)
         torch.cuda.synchronize()
         e = errs(np64(out), np64(ref_out))
-        print(f"tiny fp8 EP rank {r}/{G}: vs moe_forward bit-identical {torch.equal(out, ref_out)}, "
+        print(f"tiny fp8 (pow2 {pow2}) EP rank {r}/{G}: vs moe_forward bit-identical {torch.equal(out, ref_out)}, "
               f"out_err {e['out_err']:.2e} Frobenius {e['fro']:.2e}")
         assert torch.equal(out, ref_out)
