@@ -405,9 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (live && sub < k) {
         const int t = tok0 + row;
-        topk_idx[(size_t)t * k + sub] = my_e;
-        topk_gate[(size_t)t * k + sub] = __fdiv_rn(my_s, sum);
-        atomicAdd(&s_hist[my_e], 1);
+        if (my_e >= 0 && my_e < E) {
+          topk_idx[(size_t)t * k + sub] = my_e;
+          topk_gate[(size_t)t * k + sub] = __fdiv_rn(my_s, sum);
+          atomicAdd(&s_hist[my_e], 1);
+        } else {  // fewer than k entries: cannot happen for k <= E
+          set_error(status, status + 1, MOE_ERR_DEVICE, kSiteRouterEpi);
+        }
       }
     }
   } else if (!*abort_flag) {
