@@ -46,9 +46,10 @@ constexpr int kThreads = 32 * (9 + kProducers);  // + MMA warp 1 and epilogue wa
 static_assert(kStages % kProducers == 0, "a producer warp owns whole operand stages");
 constexpr int kKStagger = 5;                  // K-block offset between consecutive feature blocks
 constexpr uint32_t kATile = 128 * 128;        // 128 weight rows x 128 K bytes
-constexpr uint32_t kBTile = 128 * 128;        // this CTA's half of <= 224 token rows: one 128-row box
+constexpr int kBRows = kChunk / 2;            // this CTA's half of the tile's token rows
+constexpr uint32_t kBTile = kBRows * 128;     // one kBRows-row box
 constexpr uint32_t kSfTile = 2048;            // scale tile: A gate, A up, B chunk 0, B chunk 1 (512 B each)
-constexpr uint32_t kStage = 2 * kATile + kBTile + kSfTile;  // 50 KB
+constexpr uint32_t kStage = 2 * kATile + kBTile + kSfTile;  // 46 KB
 constexpr int kStgStride = 136;               // bf16 staging row stride (elements)
 constexpr uint32_t kStgBytes = 2 * 32 * kStgStride * 2;  // one [32][136] bf16 tile per epilogue group
 constexpr uint32_t kCtrl = 2048;
@@ -205,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       TileInfo ti;
       if (!decode_tile(groups, tile_start, G, E, tile, MODE, ti, cur)) continue;
       const int half = ((ti.n + 15) & ~15) / 2;  // token rows per CTA (multiple of 8)
-      const uint32_t bytes_pair = 2 * (2 * kATile + kBTile);  // both CTAs: two A blocks, one 128-row B box
+      const uint32_t bytes_pair = 2 * (2 * kATile + kBTile);  // both CTAs: two A blocks, one B box
       int a0, a1;
       a_rows(MODE, ti.mp, rank, I, a0, a1);
       const CUtensorMap* mb = ti.shared_b ? &map_b1 : &map_b0;
@@ -270,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_3d_pair(st, &map_w, fb, kq * 128, a0, ti.expert);
             tma_load_3d_pair(st + kATile, &map_w, fb, kq * 128, a1, ti.expert);
           }
-          // this CTA's token rows (up to 112 used) as one 128-row box
+          // this CTA's token rows as one kBRows-row box
           tma_load_2d_pair(st + 2 * kATile, mb, fb, kq * 128, brow);
           last_round[s] = r;
         }
@@ -551,15 +552,15 @@ moe_status_t launch_expert_ffn_mx(const moe_shape_t& s, const void* x_perm, cons
   // gate and up rows of a tile in one load: the up block is I rows after the gate block
   if (!make_map_pair_rows(&m_wgu_p, w_gate_up, u8, 1, s.d, s.I, s.I, G, 2 * (uint64_t)s.I, 128))
     return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_x, xq, u8, 1, s.d, s.T, 128, 128)) return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_xp, x_perm, u8, 1, s.d, Tk, 128, 128)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_x, xq, u8, 1, s.d, s.T, 128, kBRows)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_xp, x_perm, u8, 1, s.d, Tk, 128, kBRows)) return MOE_ERR_CUDA;
   if (!make_map_3d(&m_wd, w_down, u8, 1, s.I, s.d, G, 128, 128)) return MOE_ERR_CUDA;
   // the two channel blocks of a 512-channel tile in one load (when d is a multiple of 512)
   const int dn_pair = s.d % 512 == 0 ? 2 : 0;
   m_wd_p = m_wd;
   if (dn_pair && !make_map_pair_rows5(&m_wd_p, w_down, u8, 1, s.I, 256, 256, s.d / 512, 512, G, s.d, 128))
     return MOE_ERR_CUDA;
-  if (!make_map_2d(&m_h, hq, u8, 1, s.I, rows, 128, 128)) return MOE_ERR_CUDA;
+  if (!make_map_2d(&m_h, hq, u8, 1, s.I, rows, 128, kBRows)) return MOE_ERR_CUDA;
 
   auto k_gu = expert_gemm_mx_kernel<kGateUp>;
   auto k_dn = expert_gemm_mx_kernel<kDown>;
