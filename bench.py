@@ -268,7 +268,7 @@ def _setup_dist():
 
 
 def _config_obj(cfg, world):
-    """The `config` object both arms print (so the driver sees the same workload)."""
+    """The `config` object both arms print: one workload description for the GPU and oracle arms."""
     return {"workload": f"{cfg.name}: T={cfg.T}/GPU d={cfg.d} E={cfg.E}+{cfg.S} top-{cfg.k} I={cfg.I}",
             "global_batch": world * cfg.T, "parallelism": f"dp{world} (token-sharded replicas)",
             "l2": _l2_note(cfg)}
