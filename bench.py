@@ -230,9 +230,9 @@ class _View:
 
 
 def _traffic(cfg):
-    """DRAM bytes per step of the two expert-GEMM launches at the full V3 shape, from the ncu
-    slice captures recorded in profiles/expert_ffn_traffic.json (scaled to the full launch
-    by its algorithmic bytes) -- None for another shape, or once the kernel sources changed."""
+    """DRAM bytes per step of the two expert-GEMM launches at the full V3 shape, from the
+    full-size one-pass ncu captures recorded in profiles/expert_ffn_traffic.json -- None for
+    another shape, or once the kernel sources differ from those the capture was taken on."""
     import hashlib
 
     if (cfg.T, cfg.d, cfg.E, cfg.S, cfg.k, cfg.I) not in ((8192, 7168, 256, 1, 8, 2048), (16384, 7168, 256, 1, 8, 2048)):
