@@ -41,6 +41,7 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kChunk = kChunkMxMax;           // tokens per tile (N)
 constexpr int kMine = kChunk / 64;            // 32-column chunks per epilogue group, at most
+static_assert((kChunk + 31) / 32 <= 2 * kMine, "each epilogue group holds all of its column chunks");
 constexpr int kProducers = 2;                 // producer warps: 0 and 10 .. 8 + kProducers (4 measured slower)
 constexpr int kThreads = 32 * (9 + kProducers);  // + MMA warp 1 and epilogue warps 2-9
 static_assert(kStages % kProducers == 0, "a producer warp owns whole operand stages");
